@@ -1,0 +1,135 @@
+"""CPU oracle for paged decode attention (test infrastructure).
+
+Only tests, the smoke check and the benchmark's CPU-baseline leg may import
+this package.  The product path (the CUDA library and its Python binding)
+never imports, loads or calls it, and it imports nothing from the product.
+
+The arithmetic lives in ``pkv_oracle.c`` (plain C, fp64, one loop per term of
+the definition); this module compiles it with gcc on first use and marshals
+numpy arrays into it.  bf16 tensors are uint16 arrays of raw bf16 bits.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libpkv_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, no FMA contraction) if stale."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    stale = force or not os.path.exists(_LIB_PATH) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    )
+    if stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
+             "-std=c11", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i64, i32, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_float
+            lib.oracle_store_kvcache.restype = i64
+            lib.oracle_store_kvcache.argtypes = [P, P, P, P, P, i64, i32, i32, i64, i32]
+            lib.oracle_paged_attn_decode_pairs.restype = i64
+            lib.oracle_paged_attn_decode_pairs.argtypes = [
+                P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32, f32, P, i64, P]
+            lib.oracle_paged_attn_decode.restype = i64
+            lib.oracle_paged_attn_decode.argtypes = [
+                P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32, f32, P]
+            lib.oracle_dense_attn.restype = None
+            lib.oracle_dense_attn.argtypes = [P, P, P, i32, i32, i32, i32, f32, P]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def store_kvcache(k, v, k_cache, v_cache, slot_mapping):
+    """Scatter new K/V rows into copies of the caches.
+
+    Returns ``(k_cache_out, v_cache_out, n_out_of_range)``; inputs untouched.
+    """
+    lib = _load()
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    kc = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+    slots = _c(slot_mapping, np.int64)
+    NB, bs, Hkv, D = kc.shape
+    N = slots.shape[0]
+    assert k.shape == (N, Hkv, D) and v.shape == (N, Hkv, D)
+    bad = lib.oracle_store_kvcache(_ptr(k), _ptr(v), _ptr(kc), _ptr(vc), _ptr(slots),
+                                   N, Hkv, D, NB, bs)
+    return kc, vc, int(bad)
+
+
+def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, pairs=None):
+    """fp64 decode attention.
+
+    Without ``pairs`` returns ``[B, Hq, D]``; with ``pairs`` (an ``[n, 2]``
+    array of (b, h)) returns ``[n, D]`` for just those rows.
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = kc.shape
+    assert D2 == D and vc.shape == kc.shape and Hq % Hkv == 0
+    MBS = bt.shape[1]
+    if pairs is None:
+        out = np.zeros((B, Hq, D), dtype=np.float64)
+        bad = lib.oracle_paged_attn_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), MBS, _ptr(cl),
+                                           B, Hq, Hkv, D, NB, bs, float(scale), _ptr(out))
+    else:
+        pr = _c(pairs, np.int32).reshape(-1, 2)
+        out = np.zeros((pr.shape[0], D), dtype=np.float64)
+        bad = lib.oracle_paged_attn_decode_pairs(
+            _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), MBS, _ptr(cl), B, Hq, Hkv, D, NB, bs,
+            float(scale), _ptr(pr), pr.shape[0], _ptr(out))
+    if bad < 0:
+        raise MemoryError("oracle allocation failed")
+    return out
+
+
+def dense_attn(q, k, v, scale):
+    """fp64 attention over contiguous K/V ``[n, Hkv, D]`` for one sequence's ``q [Hq, D]``."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    Hq, D = q.shape
+    n, Hkv, D2 = k.shape
+    assert D2 == D and v.shape == k.shape
+    out = np.zeros((Hq, D), dtype=np.float64)
+    lib.oracle_dense_attn(_ptr(q), _ptr(k), _ptr(v), n, Hq, Hkv, D, float(scale), _ptr(out))
+    return out

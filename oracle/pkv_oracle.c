@@ -1,0 +1,238 @@
+/*
+ * CPU oracle for paged decode attention over a block-paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: it exists so that tests, the smoke check and the
+ * benchmark's CPU baseline can compare the CUDA kernels with a plain,
+ * slow, obviously correct restatement of what the method computes.  It
+ * shares no code, header or table with the CUDA sources.
+ *
+ * Sources (the pages this follows):
+ *  - MinivLLM guide "HowToApproachvLLM", §4.5 (prepare_prefill/decode):
+ *    the KV cache is carved into blocks along a token axis, a block's
+ *    tokens are kv_cache[..., block_id*block_size:(block_id+1)*block_size, ...],
+ *    a new token's K/V go to the flat slot given by slot_mapping, and the
+ *    attention kernel reads KV through block_tables.
+ *  - "Nano-vLLM 源码学习(2)", §2 Config: attention heads and KV heads are
+ *    distinct counts (grouped-query attention).
+ *  - "VLLM-0.7.3 源码", §3.1: a block table maps a sequence's logical
+ *    blocks to physical blocks scattered through memory.
+ *  The pages do not write out the attention formula; this oracle takes the
+ *  plain reading: for each sequence b and query head h, the output is
+ *  softmax(scale * q . K^T) . V over the first context_lens[b] cached
+ *  tokens of KV head h / (Hq/Hkv).
+ *
+ * Layouts (row-major):
+ *   k_cache, v_cache : bf16 [NB, bs, Hkv, D]   (flat slot = block*bs + offset)
+ *   q                : bf16 [B, Hq, D]
+ *   block_tables     : int32 [B, MBS]
+ *   context_lens     : int32 [B]
+ *   k, v (new)       : bf16 [N, Hkv, D]
+ *   slot_mapping     : int64 [N], -1 = padding (skipped)
+ * bf16 values are passed as their uint16 bit patterns.
+ *
+ * Arithmetic is fp64 throughout; bf16 -> fp64 widening is exact.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double bf16_to_f64(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * store_kvcache: for every i with slot_mapping[i] >= 0, copy the bf16 bits
+ * of k[i] and v[i] (all Hkv*D elements) to flat slot slot_mapping[i], i.e.
+ * block slot/bs, offset slot%bs (MinivLLM guide §4.5: slot_mapping says where
+ * each new token's KV is written; padding slots are skipped).
+ * Returns the number of slots that were out of range [0, NB*bs) and skipped.
+ */
+int64_t oracle_store_kvcache(const uint16_t *k, const uint16_t *v,
+                             uint16_t *k_cache, uint16_t *v_cache,
+                             const int64_t *slot_mapping, int64_t N,
+                             int Hkv, int D, int64_t NB, int bs)
+{
+    int64_t bad = 0;
+    int64_t row = (int64_t)Hkv * D;
+    for (int64_t i = 0; i < N; i++) {
+        int64_t slot = slot_mapping[i];
+        if (slot == -1)
+            continue;
+        if (slot < 0 || slot >= NB * (int64_t)bs) {
+            bad++;
+            continue;
+        }
+        int64_t block = slot / bs;
+        int64_t offset = slot % bs;
+        for (int h = 0; h < Hkv; h++) {
+            for (int d = 0; d < D; d++) {
+                int64_t dst = ((block * bs + offset) * Hkv + h) * D + d;
+                int64_t src = i * row + (int64_t)h * D + d;
+                k_cache[dst] = k[src];
+                v_cache[dst] = v[src];
+            }
+        }
+    }
+    return bad;
+}
+
+/*
+ * One (sequence b, query head h) of decode attention, written out from the
+ * definition: gather the first n cached tokens of KV head kvh through the
+ * block table, score s_t = scale * sum_d q_d K_td, take w_t = exp(s_t - max s),
+ * and return sum_t w_t V_t / sum_t w_t.  n == 0 gives zeros.
+ * Returns 0, or -1 when a block-table entry needed is outside [0, NB).
+ */
+static int decode_one(const uint16_t *q, const uint16_t *k_cache,
+                      const uint16_t *v_cache, const int32_t *table, int n,
+                      int Hkv, int kvh, int D, int64_t NB, int bs,
+                      double scale, double *out, double *s)
+{
+    for (int d = 0; d < D; d++)
+        out[d] = 0.0;
+    if (n <= 0)
+        return 0;
+    /* scores */
+    for (int t = 0; t < n; t++) {
+        int64_t phys = table[t / bs];
+        if (phys < 0 || phys >= NB)
+            return -1;
+        int64_t base = ((phys * bs + t % bs) * Hkv + kvh) * (int64_t)D;
+        double dot = 0.0;
+        for (int d = 0; d < D; d++)
+            dot += bf16_to_f64(q[d]) * bf16_to_f64(k_cache[base + d]);
+        s[t] = scale * dot;
+    }
+    /* softmax weights */
+    double m = s[0];
+    for (int t = 1; t < n; t++)
+        if (s[t] > m)
+            m = s[t];
+    double l = 0.0;
+    for (int t = 0; t < n; t++) {
+        s[t] = exp(s[t] - m);
+        l += s[t];
+    }
+    /* weighted sum of V */
+    for (int t = 0; t < n; t++) {
+        int64_t phys = table[t / bs];
+        int64_t base = ((phys * bs + t % bs) * Hkv + kvh) * (int64_t)D;
+        for (int d = 0; d < D; d++)
+            out[d] += s[t] * bf16_to_f64(v_cache[base + d]);
+    }
+    for (int d = 0; d < D; d++)
+        out[d] /= l;
+    return 0;
+}
+
+/*
+ * paged_attn_decode over the listed (b, h) pairs (pairs[2*i], pairs[2*i+1]);
+ * out is [n_pairs, D] fp64.  Query head h reads KV head h / (Hq / Hkv).
+ * Returns the number of pairs that hit an invalid block-table entry (their
+ * output rows are left at zero).
+ */
+int64_t oracle_paged_attn_decode_pairs(const uint16_t *q, const uint16_t *k_cache,
+                                       const uint16_t *v_cache,
+                                       const int32_t *block_tables, int MBS,
+                                       const int32_t *context_lens, int B, int Hq,
+                                       int Hkv, int D, int64_t NB, int bs, float scale,
+                                       const int32_t *pairs, int64_t n_pairs, double *out)
+{
+    int G = Hq / Hkv;
+    int64_t bad = 0;
+    int max_n = MBS * bs;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_n > 0 ? max_n : 1));
+    if (!s)
+        return -1;
+    for (int64_t i = 0; i < n_pairs; i++) {
+        int b = pairs[2 * i];
+        int h = pairs[2 * i + 1];
+        int n = context_lens[b];
+        if (n > max_n)
+            n = max_n;
+        const uint16_t *qh = q + ((int64_t)b * Hq + h) * D;
+        const int32_t *table = block_tables + (int64_t)b * MBS;
+        if (decode_one(qh, k_cache, v_cache, table, n, Hkv, h / G, D, NB, bs,
+                       (double)scale, out + i * D, s) != 0) {
+            for (int d = 0; d < D; d++)
+                out[i * D + d] = 0.0;
+            bad++;
+        }
+    }
+    free(s);
+    (void)B;
+    return bad;
+}
+
+/* paged_attn_decode over every (b, h); out is [B, Hq, D] fp64. */
+int64_t oracle_paged_attn_decode(const uint16_t *q, const uint16_t *k_cache,
+                                 const uint16_t *v_cache, const int32_t *block_tables,
+                                 int MBS, const int32_t *context_lens, int B, int Hq,
+                                 int Hkv, int D, int64_t NB, int bs, float scale,
+                                 double *out)
+{
+    int64_t n_pairs = (int64_t)B * Hq;
+    int32_t *pairs = (int32_t *)malloc(sizeof(int32_t) * 2 * (size_t)(n_pairs > 0 ? n_pairs : 1));
+    if (!pairs)
+        return -1;
+    for (int b = 0; b < B; b++)
+        for (int h = 0; h < Hq; h++) {
+            pairs[2 * ((int64_t)b * Hq + h)] = b;
+            pairs[2 * ((int64_t)b * Hq + h) + 1] = h;
+        }
+    int64_t r = oracle_paged_attn_decode_pairs(q, k_cache, v_cache, block_tables, MBS,
+                                               context_lens, B, Hq, Hkv, D, NB, bs, scale,
+                                               pairs, n_pairs, out);
+    free(pairs);
+    return r;
+}
+
+/*
+ * Dense attention over contiguous K/V [n, Hkv, D] (no paging): the result
+ * the paged cache must reproduce, since caching history only replaces
+ * recomputing it ("从零实现vLLM系列【9】：Engine", §5: v0 recomputes the full
+ * sequence each step; a KV cache keeps past K/V instead).
+ * q is [Hq, D]; out is [Hq, D] fp64.
+ */
+void oracle_dense_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int n,
+                       int Hq, int Hkv, int D, float scale, double *out)
+{
+    int G = Hq / Hkv;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    for (int h = 0; h < Hq; h++) {
+        int kvh = h / G;
+        double *o = out + (int64_t)h * D;
+        for (int d = 0; d < D; d++)
+            o[d] = 0.0;
+        if (n <= 0)
+            continue;
+        for (int t = 0; t < n; t++) {
+            double dot = 0.0;
+            for (int d = 0; d < D; d++)
+                dot += bf16_to_f64(q[(int64_t)h * D + d]) *
+                       bf16_to_f64(k[((int64_t)t * Hkv + kvh) * D + d]);
+            s[t] = (double)scale * dot;
+        }
+        double m = s[0];
+        for (int t = 1; t < n; t++)
+            if (s[t] > m)
+                m = s[t];
+        double l = 0.0;
+        for (int t = 0; t < n; t++) {
+            s[t] = exp(s[t] - m);
+            l += s[t];
+        }
+        for (int t = 0; t < n; t++)
+            for (int d = 0; d < D; d++)
+                o[d] += s[t] * bf16_to_f64(v[((int64_t)t * Hkv + kvh) * D + d]);
+        for (int d = 0; d < D; d++)
+            o[d] /= l;
+    }
+    free(s);
+}

@@ -1,0 +1,257 @@
+"""Seeded synthetic inputs for paged decode attention.
+
+This module only *draws* inputs: context lengths, block placement, block
+tables, slot mappings and bf16 tensors.  It holds none of the arithmetic of
+the method (no scatter, no scores, no softmax); both the CUDA path and the
+CPU oracle consume what it returns.
+
+Shapes follow the serving settings the pages describe:
+
+* nano-vllm ``Config``: ``max_num_seqs=512``, ``max_model_len=4096``,
+  ``kvcache_block_size=256`` ("Nano-vLLM 源码学习(2)", §2 Config).
+* vLLM 0.7.3 parameter table: ``block_size=16``, ``max_num_seqs=256``
+  ("VLLM-0.7.3 源码", §3.3).
+* A sequence's KV lives in fixed-size physical blocks named by its
+  ``block_table``; a new decode token is written at
+  ``block_table[-1] * block_size + last_block_num_tokens - 1``
+  (MinivLLM guide, §4.5 ``prepare_decode``).
+
+All arrays are numpy.  bf16 tensors are ``uint16`` arrays holding the raw
+bf16 bit patterns (fp32 N(0,1) rounded to nearest-even), so host and device
+see identical bits.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+BF16_NAN = np.uint16(0x7FC0)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (round to nearest, ties to even); return bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = (u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to fp32 (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _randn_bf16(rng: np.random.Generator, shape) -> np.ndarray:
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    step = 1 << 24  # bounded temporaries for GB-sized caches
+    for s in range(0, n, step):
+        e = min(n, s + step)
+        out[s:e] = f32_to_bf16_bits(rng.standard_normal(e - s, dtype=np.float32))
+    return out.reshape(shape)
+
+
+@dataclasses.dataclass
+class Workload:
+    """One decode step's inputs (store first, then attend)."""
+
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    bs: int
+    NB: int
+    MBS: int
+    scale: float
+    context_lens: np.ndarray  # int32 [B]; includes the new token
+    block_tables: np.ndarray  # int32 [B, MBS]; -1 past the used blocks
+    q: np.ndarray  # u16 bf16 [B, Hq, D]
+    k_cache: np.ndarray  # u16 bf16 [NB, bs, Hkv, D]
+    v_cache: np.ndarray  # u16 bf16 [NB, bs, Hkv, D]
+    k_new: np.ndarray  # u16 bf16 [N, Hkv, D]
+    v_new: np.ndarray  # u16 bf16 [N, Hkv, D]
+    slot_mapping: np.ndarray  # int64 [N]; -1 = padding, skipped
+    recipe: str = ""
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def N(self) -> int:
+        return int(self.slot_mapping.shape[0])
+
+    def kv_bytes(self) -> int:
+        """K and V bytes over every sequence's context (logical)."""
+        return int(self.context_lens.astype(np.int64).sum()) * self.Hkv * self.D * 2 * 2
+
+    def unique_kv_bytes(self) -> int:
+        """K and V bytes of the distinct physical blocks the step reads."""
+        seen = set()
+        tok = 0
+        for b in range(self.B):
+            n = int(self.context_lens[b])
+            for j in range((n + self.bs - 1) // self.bs):
+                p = int(self.block_tables[b, j])
+                if p in seen:
+                    continue
+                seen.add(p)
+                tok += min(self.bs, n - j * self.bs)
+        return tok * self.Hkv * self.D * 2 * 2
+
+    def decode_bytes(self) -> int:
+        """Algorithmic bytes of one decode: K/V over context + q + out + table + lens."""
+        tables = sum((int(n) + self.bs - 1) // self.bs for n in self.context_lens) * 4
+        return self.kv_bytes() + 2 * self.B * self.Hq * self.D * 2 + tables + 4 * self.B
+
+    def store_bytes(self) -> int:
+        """Algorithmic bytes of one store: valid rows read + written, plus slots."""
+        nv = int((self.slot_mapping >= 0).sum())
+        return 2 * nv * self.Hkv * self.D * 2 * 2 + 8 * self.N
+
+
+def decode_slot(block_table_row: np.ndarray, ctx: int, bs: int) -> int:
+    """Slot of a sequence's newest token, as ``prepare_decode`` forms it.
+
+    ``block_table[-1] * block_size + last_block_num_tokens - 1`` where the
+    table holds exactly the used blocks (MinivLLM guide, §4.5).
+    """
+    nblocks = (ctx + bs - 1) // bs
+    last_block_num_tokens = ctx - (nblocks - 1) * bs
+    return int(block_table_row[nblocks - 1]) * bs + last_block_num_tokens - 1
+
+
+def make_workload(
+    name: str,
+    B: int,
+    Hq: int,
+    Hkv: int,
+    D: int,
+    bs: int,
+    context_lens,
+    NB: int | None = None,
+    seed: int = 0,
+    shared_prefix_tokens: int = 0,
+    pad_frac: float = 0.0,
+    poison_unused: bool = False,
+    recipe: str = "",
+    rng: np.random.Generator | None = None,
+) -> Workload:
+    """Draw one step's inputs.
+
+    Draw order: (context_lens come in) -> block permutation -> q -> k_cache
+    -> v_cache -> new k -> new v -> padding mask.  Physical blocks are a
+    seeded permutation of ``[0, NB)`` handed out in sequence order, so block
+    placement is fully fragmented.  With ``shared_prefix_tokens`` the first
+    blocks of every table are the same physical ids (prefix sharing).
+    """
+    if rng is None:
+        rng = np.random.default_rng(seed)
+    ctx = np.asarray(context_lens, dtype=np.int32).reshape(B)
+    assert (ctx >= 1).all(), "every running sequence holds at least its new token"
+    nblk = (ctx.astype(np.int64) + bs - 1) // bs
+    MBS = int(nblk.max())
+    n_shared = shared_prefix_tokens // bs
+    assert shared_prefix_tokens % bs == 0
+    own = nblk - n_shared
+    assert (own >= 1).all(), "the new token must land in a sequence's own block"
+    need = n_shared + int(own.sum())
+    if NB is None:
+        NB = int(math.ceil(1.25 * need))
+    assert NB >= need
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = np.full((B, MBS), -1, dtype=np.int32)
+    cur = 0
+    shared_ids = perm[:n_shared]
+    cur = n_shared
+    for b in range(B):
+        tables[b, :n_shared] = shared_ids
+        k = int(own[b])
+        tables[b, n_shared : n_shared + k] = perm[cur : cur + k]
+        cur += k
+    q = _randn_bf16(rng, (B, Hq, D))
+    k_cache = _randn_bf16(rng, (NB, bs, Hkv, D))
+    v_cache = _randn_bf16(rng, (NB, bs, Hkv, D))
+    k_new = _randn_bf16(rng, (B, Hkv, D))
+    v_new = _randn_bf16(rng, (B, Hkv, D))
+    slots = np.array([decode_slot(tables[b], int(ctx[b]), bs) for b in range(B)], dtype=np.int64)
+    if pad_frac > 0:
+        npad = int(math.floor(pad_frac * B + 0.5))
+        idx = rng.choice(B, size=npad, replace=False)
+        slots[idx] = -1
+    if poison_unused:
+        poison_unused_slots(k_cache, v_cache, tables, ctx, bs)
+    return Workload(
+        name=name, B=B, Hq=Hq, Hkv=Hkv, D=D, bs=bs, NB=NB, MBS=MBS,
+        scale=float(np.float32(1.0 / math.sqrt(D))),
+        context_lens=ctx, block_tables=tables, q=q, k_cache=k_cache, v_cache=v_cache,
+        k_new=k_new, v_new=v_new, slot_mapping=slots, recipe=recipe,
+    )
+
+
+def poison_unused_slots(k_cache, v_cache, tables, ctx, bs) -> None:
+    """Fill every cache slot no sequence reads (unassigned blocks, tail slots) with NaN."""
+    NB = k_cache.shape[0]
+    used = np.zeros((NB, bs), dtype=bool)
+    for b in range(tables.shape[0]):
+        n = int(ctx[b])
+        for j in range((n + bs - 1) // bs):
+            lo = j * bs
+            used[tables[b, j], : min(bs, n - lo)] = True
+    k_cache[~used] = BF16_NAN
+    v_cache[~used] = BF16_NAN
+
+
+# Serving-shaped configurations.  Index 0 is the small case the oracle
+# finishes instantly; 1..4 are the full-size steps.
+CONFIG_NAMES = [
+    "tiny_paged_decode",
+    "qwen3_0p6b_decode",
+    "vllm_bs16_8b_heads",
+    "max_concurrency",
+    "long_context_shared_prefix",
+]
+
+
+def config_workload(idx: int, seed: int = 0, poison_unused: bool = False) -> Workload:
+    """The five serving-shaped steps (seeded with ``SeedSequence([seed, idx])``)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, idx]))
+    name = CONFIG_NAMES[idx]
+    if idx == 0:
+        return make_workload(
+            name, B=4, Hq=4, Hkv=2, D=64, bs=16, context_lens=[1, 17, 40, 300], NB=64,
+            rng=rng, poison_unused=poison_unused,
+            recipe="4 seqs, ctx {1,17,40,300}, bs16, 4Q/2KV, D64, NB=64 permuted, N(0,1) bf16",
+        )
+    if idx == 1:
+        ctx = rng.integers(128, 4096, size=64, endpoint=True)
+        return make_workload(
+            name, B=64, Hq=16, Hkv=8, D=128, bs=256, context_lens=ctx, rng=rng,
+            poison_unused=poison_unused,
+            recipe="64 seqs, ctx U[128,4096], bs256, 16Q/8KV, D128, NB=ceil(1.25*used), N(0,1) bf16",
+        )
+    if idx == 2:
+        ctx = rng.integers(1, 2048, size=256, endpoint=True)
+        return make_workload(
+            name, B=256, Hq=32, Hkv=8, D=128, bs=16, context_lens=ctx, rng=rng,
+            poison_unused=poison_unused,
+            recipe="256 seqs, ctx U[1,2048], bs16, 32Q/8KV, D128, NB=ceil(1.25*used), N(0,1) bf16",
+        )
+    if idx == 3:
+        ctx = np.rint(np.exp(rng.uniform(math.log(16), math.log(4096), size=512))).astype(np.int64)
+        return make_workload(
+            name, B=512, Hq=16, Hkv=8, D=128, bs=256, context_lens=ctx, rng=rng, pad_frac=0.05,
+            poison_unused=poison_unused,
+            recipe="512 seqs, ctx logU[16,4096], bs256, 16Q/8KV, D128, 26 slots=-1, N(0,1) bf16",
+        )
+    if idx == 4:
+        return make_workload(
+            name, B=8, Hq=32, Hkv=8, D=128, bs=256, context_lens=[32768] * 8,
+            shared_prefix_tokens=8192, rng=rng, poison_unused=poison_unused,
+            recipe="8 seqs x 32768, bs256, 32Q/8KV, D128, first 8192 tokens' blocks shared",
+        )
+    raise ValueError(f"no config {idx}")
