@@ -1,0 +1,459 @@
+"""Benchmark one decode step of paged attention on GB300.
+
+A step is the whole hot path on one batch: store_kvcache of the step's new
+tokens, then paged_attn_decode (split-K decode kernel + log-sum-exp merge).
+The workload is the Qwen3-0.6B-shaped serving step: 64 sequences, 16 query /
+8 KV heads, head_dim 128, block_size 256, context lengths uniform in
+[128, 4096], shuffled physical blocks, bf16 N(0,1) data (seeded, synthetic).
+Its K/V (about 0.55 GB per step) is larger than the 129 MB L2, so no flush
+is needed between steps.
+
+Prints one JSON line.  `value` is the step's algorithmic bytes (K/V over
+every context, q, out, block-table entries, context_lens, plus the store's
+rows and slots) divided by the device time per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV GB/s & % of HBM peak; seq-steps/s (1×GB300)"
+WORKLOAD_IDX = 1  # the Qwen3-0.6B-shaped step
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ["pkv_decode.cuh", "pkv_merge.cu", "pkv_kernels.h", "pkv_ptx.cuh"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--splits", type=int, default=0, help="num_splits (0 = automatic)")
+    ap.add_argument("--config", type=int, default=WORKLOAD_IDX, help=argparse.SUPPRESS)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- helpers
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_85_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if current."""
+    path = os.path.join(ROOT, "profiles", f"paged_decode_{workload_name}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_src or not m_tr or m_src.group(1) != decode_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "samples": len(sm),
+            "reasons": sorted(reasons),
+        }
+
+
+def dist_setup(n_gpus):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def reduce_max(value: float, dist, device=None) -> float:
+    """Max of a float over ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------- CPU oracle leg
+
+
+def oracle_sample(w, seqs):
+    """Run the oracle's store + decode on sequences `seqs` of the step; return bytes moved."""
+    import oracle
+
+    sel = np.asarray(seqs)
+    slots = w.slot_mapping[sel]
+    kc, vc, _ = oracle.store_kvcache(w.k_new[sel], w.v_new[sel], w.k_cache, w.v_cache, slots)
+    pairs = np.array([(b, h) for b in sel for h in range(w.Hq)], np.int32)
+    oracle.paged_attn_decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, pairs=pairs)
+    return sample_bytes(w, sel)
+
+
+def sample_bytes(w, sel):
+    ctx = w.context_lens[sel].astype(np.int64)
+    kv = int(ctx.sum()) * w.Hkv * w.D * 2 * 2
+    qo = 2 * len(sel) * w.Hq * w.D * 2
+    tab = int(((ctx + w.bs - 1) // w.bs).sum()) * 4 + 4 * len(sel)
+    nv = int((w.slot_mapping[sel] >= 0).sum())
+    store = 2 * nv * w.Hkv * w.D * 2 * 2 + 8 * len(sel)
+    return kv + qo + tab + store
+
+
+def time_oracle(w, budget_s: float):
+    """Time the oracle on a bounded sample (a prefix of the sequences) of the step."""
+    t0 = time.perf_counter()
+    oracle_sample(w, [0])  # also compiles / loads the oracle
+    one = max(time.perf_counter() - t0, 1e-4)
+    m = int(max(1, min(w.B, budget_s / one)))
+    t0 = time.perf_counter()
+    nbytes = oracle_sample(w, list(range(m)))
+    dt = time.perf_counter() - t0
+    return {
+        "value": nbytes / dt / 1e9,
+        "unit": "GB/s",
+        "cores": 1,
+        "kind": "oracle",
+        "sample": f"store+decode of the first {m} of {w.B} sequences (all heads), fp64 C oracle, "
+                  f"single thread, {dt:.1f} s",
+    }
+
+
+# ----------------------------------------------------------------- our arm
+
+
+def run_ours(args):
+    import torch
+
+    import paged_kv_cache_85_gb300 as pkv
+    from paged_kv_cache_85_gb300 import workload as wl
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+
+    w = wl.config_workload(args.config)
+    step_bytes = w.decode_bytes() + w.store_bytes()
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    host = dict(q=bf(w.q), kn=bf(w.k_new), vn=bf(w.v_new),
+                slots=torch.from_numpy(w.slot_mapping), tables=torch.from_numpy(w.block_tables),
+                lens=torch.from_numpy(w.context_lens))
+    d = {k: v.to(dev) for k, v in host.items()}
+    kc, vc = bf(w.k_cache).to(dev), bf(w.v_cache).to(dev)
+    out = torch.empty_like(d["q"])
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    ws_bytes = pkv.decode_workspace_bytes(w.B, w.Hq, w.D, w.MBS, w.bs, args.splits)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    def attn():
+        pkv.paged_attn_decode(d["q"], kc, vc, d["tables"], d["lens"], w.scale, out,
+                              num_splits=args.splits, workspace=ws, err_flag=err)
+
+    def step():
+        pkv.store_kvcache(d["kn"], d["vn"], kc, vc, d["slots"], err_flag=err)
+        attn()
+
+    launches_per_step = (1 if w.N > 0 else 0) + 2
+
+    clocks = ClockSampler(dev.index)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize(dev)
+        clocks.start()
+        # keep the GPU busy ~1 s so the clock sampler sees the loaded state
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            for _ in range(50):
+                step()
+            torch.cuda.synchronize(dev)
+
+        # ---- timed region: exactly K steps ----
+        barrier(dist, dev)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        ms_total = e0.elapsed_time(e1)
+
+        # ---- dominant call alone: paged_attn_decode (decode kernel + merge) ----
+        n_attn = max(args.steps, 50)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_attn):
+            attn()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_attn = a0.elapsed_time(a1) / n_attn
+
+        # ---- end to end through host buffers ----
+        pin = {k: v.pin_memory() for k, v in host.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = out_h.numel() * out_h.element_size()
+        for _ in range(3):
+            for k in pin:
+                d[k].copy_(pin[k], non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for _ in range(args.steps):
+            for k in pin:
+                d[k].copy_(pin[k], non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+        x1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = x0.elapsed_time(x1) / args.steps
+    clk = clocks.stop()
+    flags = int(err.item())
+
+    ms_total = reduce_max(ms_total, dist, dev)
+    ms_attn = reduce_max(ms_attn, dist, dev)
+    ms_e2e = reduce_max(ms_e2e, dist, dev)
+    ms_step = ms_total / args.steps
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_src = load_peaks()
+    achieved = w.decode_bytes() / (ms_attn * 1e-3) / 1e9
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(w, budget_s=12.0)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)",
+        "config": {
+            "workload": w.name,
+            "num_seqs": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
+            "block_size": w.bs, "context_lens": "uniform [128, 4096]",
+            "num_blocks": w.NB, "max_blocks_per_seq": w.MBS,
+            "new_tokens_per_step": w.N, "num_splits": args.splits or "auto",
+            "step_bytes": step_bytes, "kv_bytes": w.kv_bytes(),
+            "l2": "inputs larger than L2 (no flush)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "us_per_step": round(ms_step * 1e3, 2),
+        "seq_steps_per_s": round(world * w.B / (ms_step * 1e-3), 1),
+        "pct_of_hbm_peak": {
+            "measured": round(100 * value / world / peak, 1),
+            "nominal_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 1),
+            "peak_source": peak_src,
+        },
+        "roofline": {
+            "kernel": "paged_attn_decode (split-K decode kernel + LSE merge)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
+            "traffic": profiled_traffic(w.name),
+            "algorithmic_bytes_per_launch": w.decode_bytes(),
+            "us_per_launch": round(ms_attn * 1e3, 2),
+        },
+        "e2e": {
+            "value": round(world * step_bytes / (ms_e2e * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "us_per_step": round(ms_e2e * 1e3, 2),
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "device_error_flags": flags,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+# ----------------------------------------------------------- reference arm
+
+
+def run_reference(args):
+    """The oracle as the reference arm: K timed steps of a bounded sample on host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    from paged_kv_cache_85_gb300 import workload as wl
+
+    w = wl.config_workload(args.config)
+    t0 = time.perf_counter()
+    oracle_sample(w, [0])
+    one = max(time.perf_counter() - t0, 1e-4)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    m = int(max(1, min(w.B, budget / one)))
+    seqs = list(range(m))
+    for _ in range(args.warmup):
+        oracle_sample(w, seqs)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += oracle_sample(w, seqs)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    sample = (f"each step: store+decode of the first {m} of {w.B} sequences (all heads), "
+              f"fp64 C oracle, single thread")
+    line = {
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)",
+        "config": {"workload": w.name, "num_seqs": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+                   "head_dim": w.D, "block_size": w.bs},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+/*
+ * pkv.h - C ABI of a GB300 (sm_103a) paged-KV-cache decode library.
+ *
+ * Two operations make up one decode step of PagedAttention over a
+ * block-paged KV cache:
+ *
+ *   pkv_store_kvcache    scatter the step's new K/V rows into the cache
+ *                        through slot_mapping;
+ *   pkv_paged_attn_decode for every running sequence and query head,
+ *                        softmax(scale * q . K^T) . V over the sequence's
+ *                        context_len cached tokens, gathered through its
+ *                        block table, with grouped-query head sharing.
+ *
+ * Where these come from:
+ *   - MinivLLM guide "HowToApproachvLLM", section 4.4 (allocate_kv_cache:
+ *     the cache is preallocated and carved into blocks; slot_mapping tracks
+ *     where each token is written) and section 4.5 (prepare_prefill /
+ *     prepare_decode: a block's tokens are the slice
+ *     [block_id*block_size, (block_id+1)*block_size) of the token axis;
+ *     slot_mapping holds only the new tokens; the decode slot is
+ *     block_table[-1]*block_size + last_block_num_tokens - 1; block_tables
+ *     and context_lens tell the attention kernel where to read KV), and
+ *     section 4.6 (sentinel padding of slot_mapping and context_lens).
+ *   - "Nano-vLLM 源码学习(2)", section 2 Config (kvcache_block_size 256,
+ *     max_num_seqs 512, max_model_len 4096; the decode path reads paged KV
+ *     through block_table; heads and KV heads are separate counts).
+ *   - "VLLM-0.7.3 源码", section 3.1 (block table: logical blocks mapped to
+ *     physical blocks anywhere in memory; block_size 16 by default).
+ *   The pages do not print the attention formula; the plain reading
+ *   (softmax(scale q.K^T).V over the first context_len tokens, no other
+ *   mask) is used.
+ *
+ * Conventions common to every call:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; the
+ *     library never allocates, frees or keeps device memory.
+ *   - Tensors are dense row-major; bf16 data is passed as `const void *`.
+ *     Every pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work: they never synchronise the host and never allocate,
+ *     so they can be captured into a CUDA graph.
+ *   - Argument errors are reported by the return status before any launch;
+ *     pkv_last_error() then gives a message.  Data errors found on the
+ *     device (an out-of-range slot or block id, a context length above
+ *     MBS*bs) never trap: the offending item is skipped (or clamped) and a
+ *     PKV_FLAG_* bit is OR-ed into *err_flag when err_flag is non-NULL.
+ *     err_flag is a device int32 the caller zeroes and reads back.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, Hq % Hkv != 0 ... */
+    PKV_ERR_UNSUPPORTED = 2, /* valid but not built: head_dim or group size */
+    PKV_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+    PKV_ERR_CUDA = 4         /* a CUDA runtime/driver call failed */
+} pkv_status;
+
+/* Device-side error bits OR-ed into *err_flag. */
+#define PKV_FLAG_BAD_SLOT 0x1        /* slot_mapping[i] not -1 and outside [0, NB*bs) */
+#define PKV_FLAG_BAD_BLOCK 0x2       /* a needed block_tables entry outside [0, NB) */
+#define PKV_FLAG_BAD_CONTEXT_LEN 0x4 /* context_lens[b] < 0 or > MBS*bs (clamped) */
+#define PKV_FLAG_TIMEOUT 0x8         /* an internal pipeline wait gave up (a bug) */
+
+/*
+ * pkv_store_kvcache - write the step's new K/V rows into the paged cache.
+ *
+ * For every i in [0, N) with slot_mapping[i] != -1, copies the Hkv*D bf16
+ * values of k[i] and v[i] (bit for bit) to flat slot s = slot_mapping[i],
+ * i.e. block s / bs, offset s % bs of k_cache and v_cache.  slot -1 is the
+ * padding sentinel and is skipped (MinivLLM guide 4.5/4.6).
+ *
+ *   k, v          bf16 [N, Hkv, D]            new rows (read)
+ *   k_cache,
+ *   v_cache       bf16 [NB, bs, Hkv, D]       caches (written in place)
+ *   slot_mapping  int64 [N]                   flat slots, -1 = skip
+ *   N >= 0, Hkv >= 1, D in {64, 128}, NB >= 1, bs >= 16 and bs % 16 == 0
+ *   err_flag      int32 device word or NULL   PKV_FLAG_BAD_SLOT
+ *
+ * Valid slots are expected to be distinct (the block manager never hands
+ * one slot to two tokens); with duplicates the surviving row is unspecified.
+ * N == 0 enqueues nothing and returns PKV_OK.
+ */
+pkv_status pkv_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
+                             const int64_t *slot_mapping, int64_t N, int Hkv, int D,
+                             int64_t NB, int bs, int32_t *err_flag, void *stream);
+
+/*
+ * pkv_decode_workspace_bytes - device scratch pkv_paged_attn_decode needs.
+ *
+ * The context of each sequence is cut into fixed-length partitions
+ * (split-K); every partition of a sequence with more than one writes an
+ * fp32 partial result (running max, running sum, D unnormalised outputs per
+ * query head), and a second kernel merges them by log-sum-exp.  The size
+ * depends only on the arguments given here (num_splits as passed to the
+ * decode call; 0 = automatic).  Returns 0 for invalid arguments.
+ */
+size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int MBS, int bs, int num_splits);
+
+/*
+ * pkv_paged_attn_decode - one decode step of paged attention.
+ *
+ * For each sequence b < B and query head h < Hq, with G = Hq / Hkv and
+ * n = context_lens[b]:
+ *   token t < n lives at block block_tables[b*MBS + t/bs], offset t % bs;
+ *   s_t  = scale * sum_d q[b,h,d] * k_cache[block, offset, h/G, d]
+ *   out[b,h,:] = sum_t exp(s_t - max s) v_cache[block, offset, h/G, :]
+ *                / sum_t exp(s_t - max s)
+ * computed with fp32 accumulation and an fp32 online softmax, rounded to
+ * bf16 (nearest-even).  n == 0 gives zeros.  Only the first ceil(n/bs)
+ * entries of a table row are read (the rest may be -1); slots of the last
+ * block past n are never used, whatever they hold.
+ *
+ *   q             bf16 [B, Hq, D]
+ *   k_cache,
+ *   v_cache       bf16 [NB, bs, Hkv, D]
+ *   block_tables  int32 [B, MBS]
+ *   context_lens  int32 [B], 0 <= n <= MBS*bs
+ *   scale         softmax scale (commonly 1/sqrt(D))
+ *   out           bf16 [B, Hq, D]             written
+ *   workspace     device scratch of at least
+ *                 pkv_decode_workspace_bytes(B, Hq, D, MBS, bs, num_splits)
+ *                 bytes (may be NULL when that size is 0); contents on entry
+ *                 do not matter; it is overwritten
+ *   num_splits    0 = automatic; k >= 1 = cut contexts into partitions of
+ *                 ceil(MBS*bs / k) tokens (rounded up to 64), so no
+ *                 sequence is split into more than k parts
+ *   B >= 0, Hq % Hkv == 0, Hq/Hkv in {1, 2, 4, 8}, D in {64, 128},
+ *   bs >= 16 and bs % 16 == 0, B <= 8192, NB*bs < 2^31
+ *   err_flag      int32 device word or NULL   PKV_FLAG_BAD_BLOCK |
+ *                                             PKV_FLAG_BAD_CONTEXT_LEN
+ *
+ * Call pkv_store_kvcache for the step's new tokens first on the same
+ * stream; context_lens then counts the new token.
+ */
+pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, int MBS,
+                                 const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                                 int64_t NB, int bs, float scale, void *out, void *workspace,
+                                 size_t workspace_bytes, int num_splits, int32_t *err_flag,
+                                 void *stream);
+
+/* Message describing the last non-OK status returned on this host thread. */
+const char *pkv_last_error(void);
+
+/* Name of a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/* ABI version of this library (major * 100 + minor). */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

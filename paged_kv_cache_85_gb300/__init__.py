@@ -1,1 +1,201 @@
-"""GB300-native paged decode attention (placeholder; binding added with the library)."""
+"""GB300-native paged KV-cache decode attention.
+
+Python face of the C ABI in ``include/pkv.h`` (library
+``_lib/libpkv_gb300.so``, built by ``_build.build_library``).  This module only
+marshals arguments: it reads shapes from tensor metadata, hands raw device
+pointers and the current CUDA stream to the library, and lets PyTorch own the
+device memory (including the split-K workspace).  All computation happens in
+the library's CUDA kernels; there is no CPU or PyTorch fallback, and a
+missing library is an error.
+
+    store_kvcache(k, v, k_cache, v_cache, slot_mapping)
+    paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out)
+
+Layouts: k, v ``[N, Hkv, D]``; caches ``[NB, bs, Hkv, D]``; q, out
+``[B, Hq, D]`` (all bf16, contiguous, on one CUDA device); slot_mapping int64
+``[N]`` (-1 = skip); block_tables int32 ``[B, MBS]``; context_lens int32 ``[B]``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+__all__ = [
+    "store_kvcache",
+    "paged_attn_decode",
+    "decode_workspace_bytes",
+    "load_library",
+    "library_path",
+    "PkvError",
+    "FLAG_BAD_SLOT",
+    "FLAG_BAD_BLOCK",
+    "FLAG_BAD_CONTEXT_LEN",
+    "FLAG_TIMEOUT",
+]
+
+FLAG_BAD_SLOT = 0x1
+FLAG_BAD_BLOCK = 0x2
+FLAG_BAD_CONTEXT_LEN = 0x4
+FLAG_TIMEOUT = 0x8
+
+_STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
+           3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA"}
+
+
+class PkvError(RuntimeError):
+    """A library call returned a non-OK status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is missing; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                ctypes.c_float, ctypes.c_size_t)
+        lib.pkv_store_kvcache.restype = i32
+        lib.pkv_store_kvcache.argtypes = [P, P, P, P, P, i64, i32, i32, i64, i32, P, P]
+        lib.pkv_decode_workspace_bytes.restype = sz
+        lib.pkv_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.pkv_paged_attn_decode.restype = i32
+        lib.pkv_paged_attn_decode.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32,
+                                              f32, P, P, sz, i32, P, P]
+        lib.pkv_last_error.restype = ctypes.c_char_p
+        lib.pkv_last_error.argtypes = []
+        lib.pkv_version.restype = i32
+        lib.pkv_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != 0:
+        msg = load_library().pkv_last_error().decode(errors="replace")
+        raise PkvError(status, msg)
+
+
+def _require(t, name, dtype, ndim):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_ptr(device):
+    import torch
+
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def store_kvcache(k, v, k_cache, v_cache, slot_mapping, err_flag=None):
+    """Scatter new K/V rows into the paged caches through ``slot_mapping``."""
+    import torch
+
+    _require(k, "k", torch.bfloat16, 3)
+    _require(v, "v", torch.bfloat16, 3)
+    _require(k_cache, "k_cache", torch.bfloat16, 4)
+    _require(v_cache, "v_cache", torch.bfloat16, 4)
+    _require(slot_mapping, "slot_mapping", torch.int64, 1)
+    N, Hkv, D = k.shape
+    NB, bs, Hkv2, D2 = k_cache.shape
+    if v.shape != k.shape or v_cache.shape != k_cache.shape or (Hkv2, D2) != (Hkv, D):
+        raise ValueError("store_kvcache: shape mismatch between k/v and the caches")
+    if slot_mapping.shape[0] != N:
+        raise ValueError("store_kvcache: slot_mapping length != number of rows")
+    if err_flag is not None:
+        _require(err_flag, "err_flag", torch.int32, 1)
+    lib = load_library()
+    with torch.cuda.device(k.device):
+        _check(lib.pkv_store_kvcache(
+            k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+            slot_mapping.data_ptr(), N, Hkv, D, NB, bs,
+            err_flag.data_ptr() if err_flag is not None else None, _stream_ptr(k.device)))
+
+
+def decode_workspace_bytes(B, Hq, D, MBS, bs, num_splits=0) -> int:
+    return int(load_library().pkv_decode_workspace_bytes(B, Hq, D, MBS, bs, num_splits))
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(device, stream_handle, nbytes):
+    import torch
+
+    if nbytes == 0:
+        return None
+    key = (device.index, stream_handle)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                      num_splits=0, workspace=None, err_flag=None):
+    """One decode step of paged attention; writes ``out`` in place and returns it."""
+    import torch
+
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k_cache, "k_cache", torch.bfloat16, 4)
+    _require(v_cache, "v_cache", torch.bfloat16, 4)
+    _require(block_tables, "block_tables", torch.int32, 2)
+    _require(context_lens, "context_lens", torch.int32, 1)
+    _require(out, "out", torch.bfloat16, 3)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D:
+        raise ValueError("paged_attn_decode: cache shapes do not match q")
+    if out.shape != q.shape:
+        raise ValueError("paged_attn_decode: out must have q's shape")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("paged_attn_decode: block_tables/context_lens batch != q batch")
+    MBS = block_tables.shape[1]
+    if err_flag is not None:
+        _require(err_flag, "err_flag", torch.int32, 1)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        stream = _stream_ptr(q.device)
+        need = int(lib.pkv_decode_workspace_bytes(B, Hq, D, max(MBS, 1), bs, num_splits))
+        if workspace is None:
+            workspace = _workspace(q.device, stream.value, need)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _check(lib.pkv_paged_attn_decode(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+            max(MBS, 1), context_lens.data_ptr(), B, Hq, Hkv, D, NB, bs, float(scale),
+            out.data_ptr(), ws_ptr, ws_bytes, int(num_splits),
+            err_flag.data_ptr() if err_flag is not None else None, stream))
+    return out

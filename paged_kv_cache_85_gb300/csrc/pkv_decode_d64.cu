@@ -1,0 +1,14 @@
+// Instantiations of the paged decode kernel for head_dim 64 (G = 1, 2, 4, 8).
+#include "pkv_decode.cuh"
+
+namespace pkv {
+
+cudaError_t launch_decode_d64(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                              const DecodeParams &p, int grid, size_t smem, cudaStream_t stream)
+{
+    return launch_decode_dim<64>(G, tmk, tmv, p, grid, smem, stream);
+}
+
+const void *decode_kernel_d64(int G) { return decode_kernel_ptr<64>(G); }
+
+} // namespace pkv

@@ -1,0 +1,85 @@
+"""The C-ABI library builds, loads without a GPU and exports every declared symbol."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_two_operations():
+    names = _declared()
+    assert "pkv_store_kvcache" in names and "pkv_paged_attn_decode" in names
+
+
+def test_library_exports_every_declared_symbol(cuda_lib_path):
+    lib = ctypes.CDLL(cuda_lib_path)
+    for name in _declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", cuda_lib_path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (pkv_\w+)", out))
+    assert set(_declared()) <= exported
+
+
+def test_library_needs_no_cuda_shared_objects(cuda_lib_path):
+    out = subprocess.run(["ldd", cuda_lib_path], capture_output=True, text=True).stdout
+    assert "libcudart" not in out and "libcuda.so" not in out
+
+
+def test_host_only_entry_points(cuda_lib_path):
+    lib = ctypes.CDLL(cuda_lib_path)
+    lib.pkv_version.restype = ctypes.c_int
+    assert lib.pkv_version() >= 100
+    f = lib.pkv_decode_workspace_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 6
+    # one partition per sequence -> no partials needed
+    assert f(4, 4, 64, 19, 16, 1) == 0
+    # 4096-token contexts in 256-token partitions: 16 partials of (D + 2) floats per row
+    assert f(64, 16, 128, 16, 256, 0) == 64 * 16 * 16 * 130 * 4
+    assert f(-1, 4, 64, 19, 16, 0) == 0
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    assert lib.pkv_status_string(3) == b"PKV_ERR_WORKSPACE"
+
+
+def test_argument_errors_need_no_gpu(cuda_lib_path):
+    """Bad sizes are rejected on the host, before any CUDA call."""
+    lib = ctypes.CDLL(cuda_lib_path)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.pkv_paged_attn_decode.restype = i32
+    lib.pkv_paged_attn_decode.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32,
+                                          f32, P, P, sz, i32, P, P]
+    lib.pkv_last_error.restype = ctypes.c_char_p
+    # Hq not a multiple of Hkv
+    st = lib.pkv_paged_attn_decode(None, None, None, None, 1, None, 1, 6, 4, 64, 1, 16, 1.0,
+                                   None, None, 0, 0, None, None)
+    assert st == 1 and b"multiple" in lib.pkv_last_error()
+    # head_dim 96 not built
+    st = lib.pkv_paged_attn_decode(None, None, None, None, 1, None, 1, 4, 4, 96, 1, 16, 1.0,
+                                   None, None, 0, 0, None, None)
+    assert st == 2
+    # block size not a multiple of 16
+    st = lib.pkv_paged_attn_decode(None, None, None, None, 1, None, 1, 4, 4, 64, 1, 8, 1.0,
+                                   None, None, 0, 0, None, None)
+    assert st == 2
+    # B == 0 is a no-op
+    st = lib.pkv_paged_attn_decode(None, None, None, None, 1, None, 0, 4, 4, 64, 1, 16, 1.0,
+                                   None, None, 0, 0, None, None)
+    assert st == 0
+    lib.pkv_store_kvcache.restype = i32
+    lib.pkv_store_kvcache.argtypes = [P, P, P, P, P, i64, i32, i32, i64, i32, P, P]
+    assert lib.pkv_store_kvcache(None, None, None, None, None, 0, 2, 64, 4, 16, None, None) == 0
+    assert lib.pkv_store_kvcache(None, None, None, None, None, 3, 2, 64, 4, 16, None, None) == 1
