@@ -1,7 +1,7 @@
 """Benchmark one decode step of paged attention on GB300.
 
 A step is the whole hot path on one batch: store_kvcache of the step's new
-tokens, then paged_attn_decode (split-K decode kernel + log-sum-exp merge).
+tokens, then paged_attn_decode (stream-K decode kernel + log-sum-exp merge).
 The workload is the Qwen3-0.6B-shaped serving step: 64 sequences, 16 query /
 8 KV heads, head_dim 128, block_size 256, context lengths uniform in
 [128, 4096], shuffled physical blocks, bf16 N(0,1) data (seeded, synthetic).
@@ -45,7 +45,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--splits", type=int, default=0, help="num_splits (0 = automatic)")
+    ap.add_argument("--max-ctas", type=int, default=0, help="CTA cap of the decode grid (0 = one per SM)")
     ap.add_argument("--config", type=int, default=WORKLOAD_IDX, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -245,12 +245,12 @@ def run_ours(args):
     out = torch.empty_like(d["q"])
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(dev)
-    ws_bytes = pkv.decode_workspace_bytes(w.B, w.Hq, w.D, w.MBS, w.bs, args.splits)
+    ws_bytes = pkv.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, w.MBS, w.bs, args.max_ctas)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def attn():
         pkv.paged_attn_decode(d["q"], kc, vc, d["tables"], d["lens"], w.scale, out,
-                              num_splits=args.splits, workspace=ws, err_flag=err)
+                              max_ctas=args.max_ctas, workspace=ws, err_flag=err)
 
     def step():
         pkv.store_kvcache(d["kn"], d["vn"], kc, vc, d["slots"], err_flag=err)
@@ -353,7 +353,7 @@ def run_ours(args):
             "num_seqs": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
             "block_size": w.bs, "context_lens": "uniform [128, 4096]",
             "num_blocks": w.NB, "max_blocks_per_seq": w.MBS,
-            "new_tokens_per_step": w.N, "num_splits": args.splits or "auto",
+            "new_tokens_per_step": w.N, "max_ctas": args.max_ctas or "one per SM",
             "step_bytes": step_bytes, "kv_bytes": w.kv_bytes(),
             "l2": "inputs larger than L2 (no flush)",
             "parallelism": "replicas" if world > 1 else "single GPU",
@@ -366,7 +366,7 @@ def run_ours(args):
             "peak_source": peak_src,
         },
         "roofline": {
-            "kernel": "paged_attn_decode (split-K decode kernel + LSE merge)",
+            "kernel": "paged_attn_decode (stream-K decode kernel + LSE merge)",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,

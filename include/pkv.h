@@ -95,14 +95,14 @@ pkv_status pkv_store_kvcache(const void *k, const void *v, void *k_cache, void *
 /*
  * pkv_decode_workspace_bytes - device scratch pkv_paged_attn_decode needs.
  *
- * The context of each sequence is cut into fixed-length partitions
- * (split-K); every partition of a sequence with more than one writes an
- * fp32 partial result (running max, running sum, D unnormalised outputs per
- * query head), and a second kernel merges them by log-sum-exp.  The size
- * depends only on the arguments given here (num_splits as passed to the
- * decode call; 0 = automatic).  Returns 0 for invalid arguments.
+ * Depends only on its arguments (no device query); pass the same values,
+ * including max_ctas, to the decode call.  The scratch holds the per-call
+ * box layout (a few bytes per sequence) and, for every worker of the grid,
+ * two fp32 partial results (G query rows of D outputs plus running max and
+ * sum) for the pieces of contexts that straddle workers.  Returns 0 for
+ * invalid or unsupported arguments or B == 0.
  */
-size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int MBS, int bs, int num_splits);
+size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_ctas);
 
 /*
  * pkv_paged_attn_decode - one decode step of paged attention.
@@ -118,6 +118,12 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int MBS, int bs, int num
  * entries of a table row are read (the rest may be -1); slots of the last
  * block past n are never used, whatever they hold.
  *
+ * Work split: every (sequence, KV head) context is a stream of 16-token
+ * boxes; the concatenated streams are cut into equal slices over a
+ * persistent grid (eight worker warps per CTA, one CTA per SM), and a second
+ * kernel merges, by log-sum-exp, the pieces of contexts that straddle
+ * workers.  Both kernels run on `stream`.
+ *
  *   q             bf16 [B, Hq, D]
  *   k_cache,
  *   v_cache       bf16 [NB, bs, Hkv, D]
@@ -126,14 +132,15 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int MBS, int bs, int num
  *   scale         softmax scale (commonly 1/sqrt(D))
  *   out           bf16 [B, Hq, D]             written
  *   workspace     device scratch of at least
- *                 pkv_decode_workspace_bytes(B, Hq, D, MBS, bs, num_splits)
- *                 bytes (may be NULL when that size is 0); contents on entry
- *                 do not matter; it is overwritten
- *   num_splits    0 = automatic; k >= 1 = cut contexts into partitions of
- *                 ceil(MBS*bs / k) tokens (rounded up to 64), so no
- *                 sequence is split into more than k parts
+ *                 pkv_decode_workspace_bytes(B, Hq, Hkv, D, MBS, bs, max_ctas)
+ *                 bytes; contents on entry do not matter; it is overwritten,
+ *                 so calls that may overlap need separate workspaces
+ *   max_ctas      0 = as many CTAs as the device holds at once (up to 256);
+ *                 k >= 1 = at most k CTAs (moves where contexts are split;
+ *                 results agree within rounding)
  *   B >= 0, Hq % Hkv == 0, Hq/Hkv in {1, 2, 4, 8}, D in {64, 128},
- *   bs >= 16 and bs % 16 == 0, B <= 8192, NB*bs < 2^31
+ *   bs >= 16 and bs % 16 == 0, B <= 8192, NB*bs < 2^31,
+ *   B*Hkv*ceil(MBS*bs/16) < 2^31
  *   err_flag      int32 device word or NULL   PKV_FLAG_BAD_BLOCK |
  *                                             PKV_FLAG_BAD_CONTEXT_LEN
  *
@@ -144,7 +151,7 @@ pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void 
                                  const int32_t *block_tables, int MBS,
                                  const int32_t *context_lens, int B, int Hq, int Hkv, int D,
                                  int64_t NB, int bs, float scale, void *out, void *workspace,
-                                 size_t workspace_bytes, int num_splits, int32_t *err_flag,
+                                 size_t workspace_bytes, int max_ctas, int32_t *err_flag,
                                  void *stream);
 
 /* Message describing the last non-OK status returned on this host thread. */

@@ -79,7 +79,7 @@ def load_library():
         lib.pkv_store_kvcache.restype = i32
         lib.pkv_store_kvcache.argtypes = [P, P, P, P, P, i64, i32, i32, i64, i32, P, P]
         lib.pkv_decode_workspace_bytes.restype = sz
-        lib.pkv_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.pkv_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         lib.pkv_paged_attn_decode.restype = i32
         lib.pkv_paged_attn_decode.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32,
                                               f32, P, P, sz, i32, P, P]
@@ -143,8 +143,9 @@ def store_kvcache(k, v, k_cache, v_cache, slot_mapping, err_flag=None):
             err_flag.data_ptr() if err_flag is not None else None, _stream_ptr(k.device)))
 
 
-def decode_workspace_bytes(B, Hq, D, MBS, bs, num_splits=0) -> int:
-    return int(load_library().pkv_decode_workspace_bytes(B, Hq, D, MBS, bs, num_splits))
+def decode_workspace_bytes(B, Hq, Hkv, D, MBS, bs, max_ctas=0) -> int:
+    """Workspace bytes paged_attn_decode needs for these sizes (0 when B == 0)."""
+    return int(load_library().pkv_decode_workspace_bytes(B, Hq, Hkv, D, MBS, bs, max_ctas))
 
 
 _ws_cache: dict = {}
@@ -164,7 +165,7 @@ def _workspace(device, stream_handle, nbytes):
 
 
 def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
-                      num_splits=0, workspace=None, err_flag=None):
+                      max_ctas=0, workspace=None, err_flag=None):
     """One decode step of paged attention; writes ``out`` in place and returns it."""
     import torch
 
@@ -188,7 +189,7 @@ def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ou
     lib = load_library()
     with torch.cuda.device(q.device):
         stream = _stream_ptr(q.device)
-        need = int(lib.pkv_decode_workspace_bytes(B, Hq, D, max(MBS, 1), bs, num_splits))
+        need = int(lib.pkv_decode_workspace_bytes(B, Hq, Hkv, D, max(MBS, 1), bs, max_ctas))
         if workspace is None:
             workspace = _workspace(q.device, stream.value, need)
         ws_ptr = workspace.data_ptr() if workspace is not None else None
@@ -196,6 +197,6 @@ def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ou
         _check(lib.pkv_paged_attn_decode(
             q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
             max(MBS, 1), context_lens.data_ptr(), B, Hq, Hkv, D, NB, bs, float(scale),
-            out.data_ptr(), ws_ptr, ws_bytes, int(num_splits),
+            out.data_ptr(), ws_ptr, ws_bytes, int(max_ctas),
             err_flag.data_ptr() if err_flag is not None else None, stream))
     return out

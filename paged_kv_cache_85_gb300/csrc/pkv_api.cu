@@ -1,5 +1,5 @@
-// C ABI of the paged KV-cache decode library: argument checks, partition
-// choice, TMA descriptors, grid sizing and kernel launches.  Nothing here
+// C ABI of the paged KV-cache decode library: argument checks, launch
+// planning, TMA descriptors, grid sizing and kernel launches.  Nothing here
 // allocates device memory or synchronises the host.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -43,6 +43,7 @@ bool group_supported(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kMaxDynSmem = 227 * 1024;
+constexpr int kMaxGrid = 256;  // CTAs of one decode launch (one per SM)
 
 struct DeviceState {
     bool ready = false;
@@ -105,11 +106,88 @@ pkv_status make_cache_map(CUtensorMap *map, const void *cache, long long tokens,
     return PKV_OK;
 }
 
-size_t workspace_bytes_for(int B, int Hq, int D, int S)
+// Launch plan of one decode call: pipeline depth, shared memory, grid and
+// workspace layout.  The workspace query and the launch share it, so they
+// always agree.
+struct DecodePlan {
+    int G = 0, stages = 0, grid = 0;
+    size_t smem = 0, hdr_bytes = 0, ws_bytes = 0;
+    const void *kernel = nullptr;
+};
+
+pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_ctas,
+                       bool with_device, DecodePlan *plan)
 {
-    if (S <= 1)
-        return 0;
-    return pkv::align_up((size_t)B * Hq * S * (size_t)(D + 2) * 4, 256);
+    if (B < 1 || Hq < 1 || Hkv < 1 || MBS < 1 || bs < 1 || max_ctas < 0)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "paged_attn_decode: bad sizes B=%d Hq=%d Hkv=%d MBS=%d bs=%d max_ctas=%d", B, Hq,
+                    Hkv, MBS, bs, max_ctas);
+    if (Hq % Hkv != 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
+    const int G = Hq / Hkv;
+    if (!group_supported(G))
+        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: Hq/Hkv=%d not in {1,2,4,8}", G);
+    if (D != 64 && D != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: head_dim %d not in {64,128}", D);
+    if (bs % pkv::kBox != 0)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: block_size %d not a multiple of 16", bs);
+    if (B > pkv::kMaxBatch)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: B=%d above %d", B, pkv::kMaxBatch);
+    if ((long long)MBS * bs >= 0x7fffffffLL)
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: MBS*bs must be < 2^31");
+    const long long box_max = (long long)B * Hkv * (((long long)MBS * bs + pkv::kBox - 1) / pkv::kBox);
+    if (box_max >= 0x7fffffffLL)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: B*Hkv*MBS*bs/16 must be < 2^31");
+    const int stages = pkv::decode_stages_for(D, G, B, kMaxDynSmem);
+    if (stages == 0)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: B=%d does not fit shared memory", B);
+    // The workspace is sized for the largest grid the launch may use, which
+    // depends only on the arguments: one CTA per SM, at most kMaxGrid CTAs,
+    // and no more than the boxes can keep busy.
+    long long grid_cap = (box_max + pkv::kWorkers - 1) / pkv::kWorkers;
+    if (grid_cap > kMaxGrid)
+        grid_cap = kMaxGrid;
+    if (max_ctas > 0 && grid_cap > max_ctas)
+        grid_cap = max_ctas;
+    if (grid_cap < 1)
+        grid_cap = 1;
+    plan->G = G;
+    plan->stages = stages;
+    plan->smem = pkv::decode_smem_layout(D, G, stages, B).total;
+    plan->hdr_bytes = pkv::align_up((size_t)(pkv::kWsHeaderInts + B + 1) * 4, 256);
+    plan->ws_bytes = plan->hdr_bytes +
+                     (size_t)grid_cap * pkv::kWorkers * 2 * G * (size_t)(D + 4) * sizeof(float);
+    plan->grid = (int)grid_cap;
+    if (!with_device)
+        return PKV_OK;
+    DeviceState *st = nullptr;
+    pkv_status ps = device_state(&st);
+    if (ps != PKV_OK)
+        return ps;
+    const void *kfn = D == 128 ? pkv::decode_kernel_d128(G) : pkv::decode_kernel_d64(G);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        bool &set = st->smem_set[D == 128][G];
+        if (!set) {
+            cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)kMaxDynSmem);
+            if (e != cudaSuccess)
+                return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            set = true;
+        }
+    }
+    int occ = 0;
+    cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kfn, pkv::kDecodeThreads, plan->smem);
+    if (e != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+    if (occ < 1)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: kernel does not fit on an SM");
+    const long long resident = (long long)st->sms * occ;
+    if (resident < plan->grid)
+        plan->grid = (int)resident;
+    plan->kernel = kfn;
+    return PKV_OK;
 }
 
 } // namespace
@@ -161,93 +239,46 @@ pkv_status pkv_store_kvcache(const void *k, const void *v, void *k_cache, void *
     return PKV_OK;
 }
 
-size_t pkv_decode_workspace_bytes(int B, int Hq, int D, int MBS, int bs, int num_splits)
+size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_ctas)
 {
-    if (B < 0 || Hq < 1 || D < 1 || MBS < 1 || bs < 1 || num_splits < 0)
+    DecodePlan plan;
+    if (B == 0 || plan_decode(B, Hq, Hkv, D, MBS, bs, max_ctas, false, &plan) != PKV_OK)
         return 0;
-    int chunk = 0, S = 0;
-    pkv::choose_partition(MBS, bs, num_splits, &chunk, &S);
-    return workspace_bytes_for(B, Hq, D, S);
+    return plan.ws_bytes;
 }
 
 pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void *v_cache,
                                  const int32_t *block_tables, int MBS,
                                  const int32_t *context_lens, int B, int Hq, int Hkv, int D,
                                  int64_t NB, int bs, float scale, void *out, void *workspace,
-                                 size_t workspace_bytes, int num_splits, int32_t *err_flag,
+                                 size_t workspace_bytes, int max_ctas, int32_t *err_flag,
                                  void *stream)
 {
-    if (B < 0 || Hq < 1 || Hkv < 1 || MBS < 1 || NB < 1 || bs < 1 || num_splits < 0)
-        return fail(PKV_ERR_INVALID_ARG,
-                    "paged_attn_decode: bad sizes B=%d Hq=%d Hkv=%d MBS=%d NB=%lld bs=%d splits=%d",
-                    B, Hq, Hkv, MBS, (long long)NB, bs, num_splits);
-    if (Hq % Hkv != 0)
-        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
-    const int G = Hq / Hkv;
-    if (!group_supported(G))
-        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: Hq/Hkv=%d not in {1,2,4,8}", G);
-    if (D != 64 && D != 128)
-        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: head_dim %d not in {64,128}", D);
-    if (bs % pkv::kBox != 0)
-        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: block_size %d not a multiple of 16", bs);
-    if ((long long)NB * bs >= 0x7fffffffLL || (long long)MBS * bs >= 0x7fffffffLL)
-        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: NB*bs and MBS*bs must be < 2^31");
-    if (B > pkv::kMaxBatch)
-        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: B=%d above %d", B, pkv::kMaxBatch);
+    if (B < 0 || NB < 1)
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: bad sizes B=%d NB=%lld", B, (long long)NB);
     if (!std::isfinite(scale))
         return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: scale is not finite");
-    if (B == 0)
+    if (B == 0) {
+        // validate the remaining sizes even though there is nothing to do
+        if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+            return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: bad head counts");
         return PKV_OK;
+    }
+    if ((long long)NB * bs >= 0x7fffffffLL)
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: NB*bs must be < 2^31");
+    DecodePlan plan;
+    pkv_status ps = plan_decode(B, Hq, Hkv, D, MBS, bs, max_ctas, true, &plan);
+    if (ps != PKV_OK)
+        return ps;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
         return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: null pointer");
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         !aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
         (reinterpret_cast<uintptr_t>(context_lens) & 3u))
         return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: misaligned pointer");
-
-    int chunk = 0, S = 0;
-    pkv::choose_partition(MBS, bs, num_splits, &chunk, &S);
-    const size_t need = workspace_bytes_for(B, Hq, D, S);
-    if (need > 0 && (!workspace || workspace_bytes < need))
-        return fail(PKV_ERR_WORKSPACE, "paged_attn_decode: workspace needs %zu bytes, got %zu", need,
-                    workspace ? workspace_bytes : (size_t)0);
-
-    const size_t smem = pkv::decode_smem_layout(D, G, D == 128 ? pkv::DecodeShape<128>::kStages
-                                                               : pkv::DecodeShape<64>::kStages,
-                                                B, S)
-                            .total;
-    if (smem > kMaxDynSmem)
-        return fail(PKV_ERR_UNSUPPORTED,
-                    "paged_attn_decode: B=%d with %d partitions needs %zu B of shared memory", B, S,
-                    smem);
-
-    DeviceState *st = nullptr;
-    pkv_status ps = device_state(&st);
-    if (ps != PKV_OK)
-        return ps;
-    const void *kfn = D == 128 ? pkv::decode_kernel_d128(G) : pkv::decode_kernel_d64(G);
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        bool &set = st->smem_set[D == 128][G];
-        if (!set) {
-            cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)kMaxDynSmem);
-            if (e != cudaSuccess)
-                return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            set = true;
-        }
-    }
-    int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kfn, pkv::kDecodeThreads, smem);
-    if (e != cudaSuccess)
-        return fail(PKV_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
-    if (occ < 1)
-        return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: kernel does not fit on an SM");
-
-    const long long units_max = (long long)B * Hkv * S;
-    long long grid = (long long)st->sms * occ;
-    if (grid > units_max)
-        grid = units_max;
+    if (!workspace || workspace_bytes < plan.ws_bytes)
+        return fail(PKV_ERR_WORKSPACE, "paged_attn_decode: workspace needs %zu bytes, got %zu",
+                    plan.ws_bytes, workspace ? workspace_bytes : (size_t)0);
 
     CUtensorMap tmk, tmv;
     const long long tokens = (long long)NB * bs;
@@ -261,25 +292,24 @@ pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void 
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.out = static_cast<uint16_t *>(out);
-    p.ws_acc = S > 1 ? static_cast<float *>(workspace) : nullptr;
-    p.ws_ml = S > 1 ? static_cast<float *>(workspace) + (size_t)B * Hq * S * D : nullptr;
+    p.ws_hdr = static_cast<int32_t *>(workspace);
+    p.ws_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan.hdr_bytes);
     p.err_flag = err_flag;
     p.B = B;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.MBS = MBS;
     p.bs = bs;
-    p.chunk = chunk;
-    p.S = S;
     p.NB = (int)NB;
+    p.stages = plan.stages;
     p.scale_log2 = scale * 1.4426950408889634f;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    e = D == 128 ? pkv::launch_decode_d128(G, &tmk, &tmv, p, (int)grid, smem, s)
-                 : pkv::launch_decode_d64(G, &tmk, &tmv, p, (int)grid, smem, s);
+    cudaError_t e = D == 128 ? pkv::launch_decode_d128(plan.G, &tmk, &tmv, p, plan.grid, plan.smem, s)
+                             : pkv::launch_decode_d64(plan.G, &tmk, &tmv, p, plan.grid, plan.smem, s);
     if (e != cudaSuccess)
         return fail(PKV_ERR_CUDA, "paged_attn_decode launch: %s", cudaGetErrorString(e));
-    e = pkv::launch_merge(D, p, s);
+    e = pkv::launch_merge(D, plan.G, p, s);
     if (e != cudaSuccess)
         return fail(PKV_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
     return PKV_OK;

@@ -8,35 +8,34 @@
 // h / (Hq / Hkv).
 //
 // How (GB300 design):
-//  * Split-K.  Each sequence's context is cut into partitions of `chunk`
-//    tokens.  A work unit is one (partition, sequence, KV head); all G query
-//    heads sharing that KV head are handled together, so every K/V byte is
-//    read from HBM once.  Units are enumerated partition-major (all
-//    sequences' first partitions, then the second ones, ...), which keeps
-//    sequences that share prefix blocks reading them at the same time, and
-//    they are dealt round-robin to a persistent grid of CTAs sized to fill
-//    the 152 SMs.  Each CTA rebuilds the unit map from context_lens in
-//    shared memory (a histogram + prefix sum), so the host never reads
-//    context lengths and the call needs no host synchronisation.
-//  * Producer warp.  One warp walks the CTA's units, resolves the block
-//    table 32 boxes ahead (one coalesced load per 512 tokens, prefetched one
-//    segment in advance), and issues TMA copies of 16-token boxes of K and V
-//    ([16 tokens x D] bf16 from the [NB*bs, Hkv, D] cache view) into a ring
-//    of shared-memory stages, each completed on an mbarrier with its byte
-//    count.  The unit's G query rows come in with its first tile by a bulk
-//    copy.
-//  * Consumer warps (4).  Each takes one 16-token box of every 64-token
-//    stage.  Scores: 8 lanes share a token (16 B vector loads of the K row,
-//    conflict-free), each lane dots its slice of d with all G query rows in
-//    packed fp32 FMAs, then a reduce-scatter across the 8 lanes leaves one
-//    (token, head) score per lane.  Online softmax in fp32 (log2 domain,
-//    running max and sum per head), probabilities go through a tiny shared
-//    buffer, and P.V accumulates in packed fp32 FMAs with each lane owning
-//    D/32 output columns of all G heads.  At the end of a unit the four
-//    warps' partial states are merged (log-sum-exp) in shared memory; a
-//    sequence with one partition is normalised and written as bf16, one
-//    with several writes (acc, max, sum) to the workspace for the merge
-//    kernel.
+//  * Work decomposition (stream-K).  Each (sequence, KV head) context is a
+//    stream of 16-token boxes; all G query heads of the group ride along, so
+//    every K/V byte is read from HBM once.  The streams are concatenated
+//    (sequence-major) and the resulting box range is cut into equal
+//    contiguous slices, one per worker; a worker is one consumer warp, and a
+//    persistent grid of CTAs with eight workers each fills the 152 SMs.
+//    Every worker therefore moves the same number of bytes (+-1 box), and a
+//    stream is split only where a slice boundary falls into it.  Each CTA
+//    rebuilds the per-sequence box prefix sums from context_lens in shared
+//    memory, so the host never reads context lengths and the call needs no
+//    host synchronisation.
+//  * Producer warp.  Lane w runs worker w: every pipeline stage carries one
+//    box per worker, and each lane walks its worker's slice, loading block
+//    ids four boxes ahead of use, so no copy waits on a block-table read.  Boxes ([16 tokens x D] bf16 of one KV head, from
+//    the [NB*bs, Hkv, D] cache view) arrive by TMA into a ring of
+//    shared-memory stages completed on mbarriers with their byte counts; the
+//    G query rows of a worker's new piece come with it by a bulk copy.
+//  * Consumer warps (workers).  Scores: 8 lanes share a token (16-byte,
+//    conflict-free reads of the K row); each lane dots its slice of d with
+//    all G query rows in packed fp32 FMAs, and a reduce-scatter across the
+//    8 lanes leaves one (token, head) score per lane.  Online softmax in fp32
+//    (log2 domain, running max and sum per head); probabilities go through a
+//    small per-warp buffer; P.V accumulates in packed fp32 FMAs with each
+//    lane owning D/32 output columns of all G heads.  When a worker finishes
+//    a piece of a stream it either writes the normalised bf16 output (the
+//    piece is the whole stream) or a partial (acc, max, sum) into one of its
+//    two workspace slots (first / last piece of its slice); a second kernel
+//    merges the partials of streams that straddle workers by log-sum-exp.
 //  * Masking selects out tokens at or past context_len (scores -> -inf and
 //    the P.V loop stops at the last valid token), so whatever the unused
 //    slots of the last block hold (even NaN) never reaches the output.
@@ -49,64 +48,61 @@
 
 namespace pkv {
 
-template <int D> struct DecodeShape {
-    static constexpr int kStages = D == 128 ? 3 : 6;
-    static constexpr int kRowBytes = D * 2;
-    static constexpr int kBoxBytes = kBox * kRowBytes;
-    static constexpr int kTileBytes = kTile * kRowBytes;
-};
+constexpr int kLookahead = 4;  // boxes per worker whose block ids are loaded ahead of use
 
-// Per-stage descriptor written by the producer before it arms the stage.
-struct __align__(16) StageMeta {
-    int b, h, c, nvalid;
-    int flags;
-    int pad[3];
+// Per-worker box descriptor of a stage, written by the producer.
+struct __align__(16) BoxMeta {
+    int b, h, tok0, nvalid;
+    int flags, blk, pad0, pad1;
 };
-constexpr int kMetaFirst = 1;   // first tile of its unit (carries the q rows)
-constexpr int kMetaLast = 2;    // last tile of its unit
-constexpr int kMetaSingle = 4;  // the sequence has one partition: write bf16 out
-constexpr int kMetaStop = 1 << 30;
-constexpr int kMetaMaskShift = 8;  // bits 8..11: which 16-token boxes were loaded
+constexpr int kBoxValid = 1;     // the worker has a box in this stage
+constexpr int kBoxLoaded = 2;    // its K/V were copied (the block id was valid)
+constexpr int kPieceFirst = 4;   // first box of the worker's piece of this stream (q comes with it)
+constexpr int kPieceLast = 8;    // last box of the piece: finish it after this box
+constexpr int kStreamFirst = 16; // box 0 of the stream
+constexpr int kStreamLast = 32;  // last box of the stream
+constexpr int kSlot1 = 64;       // a partial of this piece goes to the worker's second slot
+constexpr int kStageStop = 1 << 30;
 
 struct DecodeSmem {
-    size_t k, v, q, acc, ml, pbuf, full, empty, meta, prefix, hist, lens, nch, total;
+    size_t kv, q, pbuf, full, empty, meta, pb, len, scan, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int stages, int B, int S)
+__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int stages, int B)
 {
     DecodeSmem L;
     size_t o = 0;
-    const size_t tile = (size_t)kTile * D * 2;
-    L.k = o;
-    o += stages * tile;
-    L.v = o;
-    o += stages * tile;
-    L.q = o;
-    o = align_up(o + (size_t)stages * G * D * 2, 16);
-    L.acc = o;
-    o = align_up(o + (size_t)kConsumerWarps * G * D * 4, 16);
-    L.ml = o;
-    o = align_up(o + (size_t)kConsumerWarps * G * 2 * 4, 16);
-    L.pbuf = o;
-    o = align_up(o + (size_t)kConsumerWarps * kBox * G * 8, 16);
+    L.kv = o;  // per stage: K boxes [kWorkers][16][D], then V boxes [kWorkers][16][D]
+    o += (size_t)stages * 2 * kWorkers * kBox * D * 2;
+    L.q = o;  // per stage and worker: G query rows
+    o = align_up(o + (size_t)stages * kWorkers * G * D * 2, 16);
+    L.pbuf = o;  // per worker: probabilities [16 tokens][G] as (p, p) pairs
+    o = align_up(o + (size_t)kWorkers * kBox * G * 8, 16);
     L.full = o;
-    o += stages * 8;
+    o += (size_t)stages * 8;
     L.empty = o;
-    o += stages * 8;
+    o += (size_t)stages * 8;
     L.meta = o = align_up(o, 16);
-    o += stages * sizeof(StageMeta);
-    L.prefix = o;
-    o = align_up(o + (size_t)(S + 1) * 4, 16);
-    L.hist = o;
-    o = align_up(o + (size_t)(S + 1) * 4, 16);
-    L.lens = o;
+    o += (size_t)stages * kWorkers * sizeof(BoxMeta);
+    L.pb = o;  // boxes per KV head before sequence b, b = 0..B
+    o = align_up(o + (size_t)(B + 1) * 4, 16);
+    L.len = o;  // clamped context length per sequence
     o = align_up(o + (size_t)B * 4, 16);
-    L.nch = o;
-    o = align_up(o + (size_t)B * 2, 16);
+    L.scan = o;  // per-warp partial sums of the prefix scan
+    o = align_up(o + (size_t)(kDecodeThreads / 32 + 1) * 4, 16);
     L.total = o;
     return L;
+}
+
+// Deepest pipeline (2..4 stages) whose shared memory fits one CTA per SM.
+inline int decode_stages_for(int D, int G, int B, size_t max_smem)
+{
+    for (int s = kMaxStages; s >= kMinStages; s--)
+        if (decode_smem_layout(D, G, s, B).total <= max_smem)
+            return s;
+    return 0;
 }
 
 // Sum of G per-lane partial values over the 8 lanes of a token group, left
@@ -152,229 +148,213 @@ template <> struct GroupLog2<2> { static constexpr int v = 1; };
 template <> struct GroupLog2<4> { static constexpr int v = 2; };
 template <> struct GroupLog2<8> { static constexpr int v = 3; };
 
-// Work unit: (partition c, sequence b, KV head h) covering tokens [t0, t1).
-struct Unit {
-    int b, h, c, t0, t1, single;
-};
-
-// Map unit index u (partition-major order) to its unit; false past the end.
-// Whole-warp call (ballot scan over the sequences).
-__device__ __forceinline__ bool map_unit(int u, const DecodeParams &p, const int *sP,
-                                         const int *sLen, const uint16_t *sN, int lane, Unit &U)
+// Box x of the concatenated streams -> (sequence b, KV head h, box j of the
+// stream).  pb[b] = boxes per KV head before sequence b; x < pb[B] * Hkv.
+__device__ __forceinline__ void locate_box(int x, const int *pb, int B, int Hkv, int &b, int &h,
+                                           int &j)
 {
-    const int total = sP[p.S] * p.Hkv;
-    if (u >= total)
-        return false;
-    const int qi = u / p.Hkv;
-    U.h = u - qi * p.Hkv;
-    int lo = 0, hi = p.S - 1;  // largest c with sP[c] <= qi
+    int lo = 0, hi = B - 1;  // largest b with pb[b] * Hkv <= x (skips empty sequences)
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (sP[mid] <= qi)
+        if (pb[mid] * Hkv <= x)
             lo = mid;
         else
             hi = mid - 1;
     }
-    const int c = lo;
-    int k = qi - sP[c];  // k-th (0-based) sequence with more than c partitions
-    int b = 0;
-    for (int base = 0; base < p.B; base += 32) {
-        const int bb = base + lane;
-        const bool act = bb < p.B && sN[bb] > c;
-        const unsigned m = __ballot_sync(0xffffffffu, act);
-        const int cnt = __popc(m);
-        if (k < cnt) {
-            b = base + (int)__fns(m, 0, k + 1);
-            break;
+    b = lo;
+    const int nb = pb[b + 1] - pb[b];
+    const int r = x - pb[b] * Hkv;
+    h = r / nb;
+    j = r - h * nb;
+}
+
+// Advance a (sequence, KV head, box) cursor to the next box of the
+// concatenated streams, skipping sequences without boxes.
+__device__ __forceinline__ void next_box(const int *pb, int B, int Hkv, int &b, int &h, int &j)
+{
+    if (++j == pb[b + 1] - pb[b]) {
+        j = 0;
+        if (++h == Hkv) {
+            h = 0;
+            ++b;
+            while (b < B && pb[b + 1] == pb[b])
+                ++b;
         }
-        k -= cnt;
-    }
-    U.b = b;
-    U.c = c;
-    U.t0 = c * p.chunk;
-    U.t1 = min(sLen[b], U.t0 + p.chunk);
-    U.single = sN[b] == 1;
-    return true;
-}
-
-// A stretch of <= kSegTokens tokens of one unit whose block ids are fetched
-// by one load per lane (lane i holds the block of box i).
-struct Seg {
-    Unit U;
-    int u, s0, s1;
-    bool valid;
-};
-
-__device__ __forceinline__ void first_seg(int u, const DecodeParams &p, const int *sP,
-                                          const int *sLen, const uint16_t *sN, int lane, Seg &s)
-{
-    s.u = u;
-    s.valid = map_unit(u, p, sP, sLen, sN, lane, s.U);
-    if (s.valid) {
-        s.s0 = s.U.t0;
-        s.s1 = min(s.U.t1, s.s0 + kSegTokens);
     }
 }
 
-__device__ __forceinline__ void next_seg(const Seg &cur, const DecodeParams &p, const int *sP,
-                                         const int *sLen, const uint16_t *sN, int lane,
-                                         Seg &n)
+__device__ __forceinline__ int box_block(const DecodeParams &p, int b, int j)
 {
-    if (cur.valid && cur.s1 < cur.U.t1) {
-        n = cur;
-        n.s0 = cur.s1;
-        n.s1 = min(cur.U.t1, n.s0 + kSegTokens);
-    } else {
-        first_seg(cur.u + (int)gridDim.x, p, sP, sLen, sN, lane, n);
-    }
+    return __ldg(p.block_tables + (size_t)b * p.MBS + (j * kBox) / p.bs);
 }
 
-__device__ __forceinline__ int load_seg_blocks(const Seg &s, const DecodeParams &p, int lane)
-{
-    const int tok = s.s0 + lane * kBox;
-    if (!s.valid || tok >= s.s1)
-        return -1;
-    return __ldg(p.block_tables + (size_t)s.U.b * p.MBS + tok / p.bs);
-}
-
+// Producer warp: lane w < kWorkers runs worker w of this CTA.  Each lane
+// walks its own slice with two cursors: the issue cursor, and a look-ahead
+// cursor kLookahead boxes further on whose block ids are loaded into a small
+// register queue, so a copy never waits on a block-table read.  Per stage
+// every lane writes its worker's box descriptor and issues its own TMA
+// copies; lane 0 arms the stage's mbarrier with the summed byte count.
 template <int D, int G>
 __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CUtensorMap *tmv,
                                                 const DecodeParams &p, uint8_t *smem,
-                                                const DecodeSmem &L, int lane)
+                                                const DecodeSmem &L, int lane, int T, int P)
 {
-    using Sh = DecodeShape<D>;
-    constexpr int STAGES = Sh::kStages;
+    constexpr unsigned FULL = 0xffffffffu;
+    constexpr int kBoxBytes = kBox * D * 2;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
-    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L.meta);
-    const int *sP = reinterpret_cast<const int *>(smem + L.prefix);
-    const int *sLen = reinterpret_cast<const int *>(smem + L.lens);
-    const uint16_t *sN = reinterpret_cast<const uint16_t *>(smem + L.nch);
+    BoxMeta *meta = reinterpret_cast<BoxMeta *>(smem + L.meta);
+    const int *pb = reinterpret_cast<const int *>(smem + L.pb);
+    const int *len = reinterpret_cast<const int *>(smem + L.len);
 
     if (lane == 0) {
         prefetch_tensormap(tmk);
         prefetch_tensormap(tmv);
     }
-    Seg cur, nxt;
-    first_seg((int)blockIdx.x, p, sP, sLen, sN, lane, cur);
-    int cur_blk = load_seg_blocks(cur, p, lane);
-    next_seg(cur, p, sP, sLen, sN, lane, nxt);
-    int nxt_blk = load_seg_blocks(nxt, p, lane);
+    const bool worker = lane < kWorkers;
+    const long long s0 = ((long long)blockIdx.x * kWorkers + lane) * P;
+    const int start = worker ? (int)(s0 < T ? s0 : T) : T;
+    const int end = worker ? (int)(s0 + P < T ? s0 + P : T) : T;
+    int pos = start;
+    int cb = 0, ch = 0, cj = 0;  // issue cursor
+    if (start < end)
+        locate_box(start, pb, p.B, p.Hkv, cb, ch, cj);
+    int lb = cb, lh = ch, lj = cj, lpos = start;  // look-ahead cursor
+    int qb[kLookahead];                          // block ids of boxes pos .. pos + kLookahead - 1
+#pragma unroll
+    for (int i = 0; i < kLookahead; i++) {
+        qb[i] = -1;
+        if (lpos < end) {
+            qb[i] = box_block(p, lb, lj);
+            next_box(pb, p.B, p.Hkv, lb, lh, lj);
+        }
+        ++lpos;
+    }
+    bool first_done = false;
 
     // K/V may have just been written by store_kvcache on this stream.
     grid_dependency_wait();
 
     int stage = 0;
     uint32_t phase = 0;
-    while (cur.valid) {
-        for (int ts = cur.s0; ts < cur.s1; ts += kTile) {
-            const int nvalid = min(kTile, cur.U.t1 - ts);
-            const int box0 = (ts - cur.s0) / kBox;
-            int blk[4];
-            int mask = 0;
-            bool bad = false;
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                blk[j] = __shfl_sync(0xffffffffu, cur_blk, (box0 + j) & 31);
-                if (j * kBox < nvalid) {
-                    if (blk[j] >= 0 && blk[j] < p.NB)
-                        mask |= 1 << j;
-                    else
-                        bad = true;
-                }
-            }
-            if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1))) {
-                if (lane == 0)
-                    flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
-                return;
-            }
-            if (lane == 0) {
-                if (bad)
-                    flag_error(p.err_flag, 0x2 /* PKV_FLAG_BAD_BLOCK */);
-                const bool first = ts == cur.U.t0;
-                const bool last = ts + kTile >= cur.U.t1;
-                StageMeta &m = meta[stage];
-                m.b = cur.U.b;
-                m.h = cur.U.h;
-                m.c = cur.U.c;
-                m.nvalid = nvalid;
-                m.flags = (first ? kMetaFirst : 0) | (last ? kMetaLast : 0) |
-                          (cur.U.single ? kMetaSingle : 0) | (mask << kMetaMaskShift);
-                const uint32_t bytes = (uint32_t)__popc(mask) * 2u * Sh::kBoxBytes +
-                                       (first ? (uint32_t)(G * D * 2) : 0u);
-                mbar_arrive_expect_tx(&full[stage], bytes);
-                if (first)
-                    bulk_load(smem + L.q + (size_t)stage * G * D * 2,
-                              p.q + ((size_t)cur.U.b * p.Hq + (size_t)cur.U.h * G) * D,
-                              G * D * 2, &full[stage]);
-                uint8_t *kd = smem + L.k + (size_t)stage * Sh::kTileBytes;
-                uint8_t *vd = smem + L.v + (size_t)stage * Sh::kTileBytes;
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    if (mask & (1 << j)) {
-                        const int tok = ts + j * kBox;
-                        const int row = blk[j] * p.bs + tok % p.bs;
-                        tma_load_3d(kd + j * Sh::kBoxBytes, tmk, 0, cur.U.h, row, &full[stage]);
-                        tma_load_3d(vd + j * Sh::kBoxBytes, tmv, 0, cur.U.h, row, &full[stage]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1;
-            }
+    for (;;) {
+        const bool mine = pos < end;
+        if (!__any_sync(FULL, mine))
+            break;
+        if (!__all_sync(FULL, mbar_wait(&empty[stage], phase ^ 1))) {
+            if (lane == 0)
+                flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
+            return;
         }
-        cur = nxt;
-        cur_blk = nxt_blk;
-        next_seg(cur, p, sP, sLen, sN, lane, nxt);
-        nxt_blk = load_seg_blocks(nxt, p, lane);
+        uint32_t bytes = 0;
+        int flags = 0, row = 0, b = cb, h = ch;
+        if (mine) {
+            const int j = cj;
+            const int blk = qb[0];
+            const int nb = pb[b + 1] - pb[b];
+            const int tok0 = j * kBox;
+            const bool loaded = blk >= 0 && blk < p.NB;
+            if (!loaded)
+                flag_error(p.err_flag, 0x2 /* PKV_FLAG_BAD_BLOCK */);
+            const bool pf = pos == start || j == 0;
+            const bool pl = pos == end - 1 || j == nb - 1;
+            flags = kBoxValid | (loaded ? kBoxLoaded : 0) | (pf ? kPieceFirst : 0) |
+                    (pl ? kPieceLast : 0) | (j == 0 ? kStreamFirst : 0) |
+                    (j == nb - 1 ? kStreamLast : 0) | (first_done ? kSlot1 : 0);
+            if (pl)
+                first_done = true;
+            bytes = (loaded ? 2u * kBoxBytes : 0u) + (pf ? (uint32_t)(G * D * 2) : 0u);
+            row = loaded ? blk * p.bs + tok0 % p.bs : 0;
+            BoxMeta &m = meta[stage * kWorkers + lane];
+            m.b = b;
+            m.h = h;
+            m.tok0 = tok0;
+            m.nvalid = min(kBox, len[b] - tok0);
+            m.flags = flags;
+            m.blk = blk;
+            // advance both cursors
+            next_box(pb, p.B, p.Hkv, cb, ch, cj);
+            ++pos;
+#pragma unroll
+            for (int i = 0; i + 1 < kLookahead; i++)
+                qb[i] = qb[i + 1];
+            qb[kLookahead - 1] = -1;
+            if (lpos < end) {
+                qb[kLookahead - 1] = box_block(p, lb, lj);
+                next_box(pb, p.B, p.Hkv, lb, lh, lj);
+            }
+            ++lpos;
+        } else if (worker) {
+            meta[stage * kWorkers + lane].flags = 0;
+        }
+        bytes = __reduce_add_sync(FULL, bytes);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive_expect_tx(&full[stage], bytes);
+        __syncwarp();
+        if (flags & kPieceFirst)
+            bulk_load(smem + L.q + ((size_t)stage * kWorkers + lane) * G * D * 2,
+                      p.q + ((size_t)b * p.Hq + (size_t)h * G) * D, G * D * 2, &full[stage]);
+        if (flags & kBoxLoaded) {
+            uint8_t *kd = smem + L.kv + ((size_t)stage * 2 * kWorkers + lane) * kBoxBytes;
+            tma_load_3d(kd, tmk, 0, h, row, &full[stage]);
+            tma_load_3d(kd + (size_t)kWorkers * kBoxBytes, tmv, 0, h, row, &full[stage]);
+        }
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1;
+        }
     }
     // Tell the consumers there is no more work.
-    if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1))) {
+    if (!__all_sync(FULL, mbar_wait(&empty[stage], phase ^ 1))) {
         if (lane == 0)
             flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
         return;
     }
-    if (lane == 0) {
-        meta[stage].flags = kMetaStop;
+    if (worker)
+        meta[stage * kWorkers + lane].flags = kStageStop;
+    __syncwarp();
+    if (lane == 0)
         mbar_arrive(&full[stage]);
-    }
 }
 
 template <int D, int G>
 __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *smem,
                                                 const DecodeSmem &L, int warp, int lane)
 {
-    using Sh = DecodeShape<D>;
-    constexpr int STAGES = Sh::kStages;
     constexpr int NCH = D / 64;      // 16-byte K chunks per lane per token (2 or 1)
     constexpr int EP = NCH * 4;      // packed fp32 pairs of q per head per lane
     constexpr int DPL = D / 32;      // output columns per lane
     constexpr int VP = DPL / 2;      // packed pairs of output columns
     constexpr int HSHIFT = 3 - GroupLog2<G>::v;
+    constexpr int kBoxBytes = kBox * D * 2;
+    constexpr int kRowBytes = D * 2;
     constexpr unsigned FULL = 0xffffffffu;
 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
-    const StageMeta *meta = reinterpret_cast<const StageMeta *>(smem + L.meta);
+    const BoxMeta *meta = reinterpret_cast<const BoxMeta *>(smem + L.meta);
     float2 *pbuf = reinterpret_cast<float2 *>(smem + L.pbuf) + warp * kBox * G;
-    float *sAcc = reinterpret_cast<float *>(smem + L.acc);
-    float *sML = reinterpret_cast<float *>(smem + L.ml);
 
     const int r = lane & 7;        // position within the 8-lane token group
     const int slot = lane >> 3;    // which of 4 tokens this lane scores per step
     const int hsel = r >> HSHIFT;  // head of this lane's score after the reduction
     const bool leader = (r & ((1 << HSHIFT) - 1)) == 0;
+    const int gw = blockIdx.x * kWorkers + warp;
 
     float2 qv[G][EP];
     float2 acc[G][VP];
     float m_run = -INFINITY, l_run = 0.f;
+    bool whole = false;  // the current piece began at its stream's first box
 #pragma unroll
-    for (int g = 0; g < G; g++)
+    for (int g = 0; g < G; g++) {
+#pragma unroll
+        for (int i = 0; i < EP; i++)
+            qv[g][i] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < VP; i++)
             acc[g][i] = make_float2(0.f, 0.f);
+    }
 
     int stage = 0;
     uint32_t phase = 0;
@@ -384,47 +364,50 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *
                 flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
             return;
         }
-        const StageMeta m = meta[stage];
-        if (m.flags & kMetaStop)
+        const BoxMeta bm = meta[stage * kWorkers + warp];
+        if (bm.flags & kStageStop)
             break;
-        const uint8_t *Ks = smem + L.k + (size_t)stage * Sh::kTileBytes + warp * Sh::kBoxBytes;
-        const uint8_t *Vs = smem + L.v + (size_t)stage * Sh::kTileBytes + warp * Sh::kBoxBytes;
-
-        if (m.flags & kMetaFirst) {
-            const uint8_t *qs = smem + L.q + (size_t)stage * G * D * 2;
+        if (bm.flags & kPieceFirst) {
+            const uint8_t *qs = smem + L.q + ((size_t)stage * kWorkers + warp) * G * D * 2;
+            const float2 sc = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
             for (int g = 0; g < G; g++)
 #pragma unroll
                 for (int ch = 0; ch < NCH; ch++) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(qs + (g * D + ch * 64 + r * 8) * 2);
-                    const float2 sc = make_float2(p.scale_log2, p.scale_log2);
-                    qv[g][ch * 4 + 0] = __fmul2_rn(bf16x2_to_float2(w.x), sc);
-                    qv[g][ch * 4 + 1] = __fmul2_rn(bf16x2_to_float2(w.y), sc);
-                    qv[g][ch * 4 + 2] = __fmul2_rn(bf16x2_to_float2(w.z), sc);
-                    qv[g][ch * 4 + 3] = __fmul2_rn(bf16x2_to_float2(w.w), sc);
+                    const uint4 w4 =
+                        *reinterpret_cast<const uint4 *>(qs + (g * D + ch * 64 + r * 8) * 2);
+                    qv[g][ch * 4 + 0] = __fmul2_rn(bf16x2_to_float2(w4.x), sc);
+                    qv[g][ch * 4 + 1] = __fmul2_rn(bf16x2_to_float2(w4.y), sc);
+                    qv[g][ch * 4 + 2] = __fmul2_rn(bf16x2_to_float2(w4.z), sc);
+                    qv[g][ch * 4 + 3] = __fmul2_rn(bf16x2_to_float2(w4.w), sc);
                 }
+            m_run = -INFINITY;
+            l_run = 0.f;
+#pragma unroll
+            for (int g = 0; g < G; g++)
+#pragma unroll
+                for (int i = 0; i < VP; i++)
+                    acc[g][i] = make_float2(0.f, 0.f);
+            whole = (bm.flags & kStreamFirst) != 0;
         }
-
-        int nvw = m.nvalid - warp * kBox;
-        nvw = nvw < 0 ? 0 : (nvw > kBox ? kBox : nvw);
-        if (!((m.flags >> (kMetaMaskShift + warp)) & 1))
-            nvw = 0;
-
+        const int nvw = (bm.flags & kBoxLoaded) ? bm.nvalid : 0;
         if (nvw > 0) {
-            // ---- scores for this warp's 16 tokens (4 per step) ----
+            const uint8_t *Ks = smem + L.kv + ((size_t)stage * 2 * kWorkers + warp) * kBoxBytes;
+            const uint8_t *Vs = Ks + (size_t)kWorkers * kBoxBytes;
+            // ---- scores for the box's 16 tokens (4 per step) ----
             float sv[4];
 #pragma unroll
             for (int j = 0; j < 4; j++) {
                 const int tt = 4 * j + slot;
-                const uint8_t *row = Ks + tt * Sh::kRowBytes;
+                const uint8_t *row = Ks + tt * kRowBytes;
                 float2 kf[EP];
 #pragma unroll
                 for (int ch = 0; ch < NCH; ch++) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(row + ch * 128 + r * 16);
-                    kf[ch * 4 + 0] = bf16x2_to_float2(w.x);
-                    kf[ch * 4 + 1] = bf16x2_to_float2(w.y);
-                    kf[ch * 4 + 2] = bf16x2_to_float2(w.z);
-                    kf[ch * 4 + 3] = bf16x2_to_float2(w.w);
+                    const uint4 w4 = *reinterpret_cast<const uint4 *>(row + ch * 128 + r * 16);
+                    kf[ch * 4 + 0] = bf16x2_to_float2(w4.x);
+                    kf[ch * 4 + 1] = bf16x2_to_float2(w4.y);
+                    kf[ch * 4 + 2] = bf16x2_to_float2(w4.z);
+                    kf[ch * 4 + 3] = bf16x2_to_float2(w4.w);
                 }
                 float part[G];
 #pragma unroll
@@ -477,11 +460,11 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *
                     }
                 }
                 float2 vf[VP];
-                const uint8_t *vrow = Vs + t * Sh::kRowBytes + lane * DPL * 2;
+                const uint8_t *vrow = Vs + t * kRowBytes + lane * DPL * 2;
                 if constexpr (VP == 2) {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(vrow);
-                    vf[0] = bf16x2_to_float2(w.x);
-                    vf[1] = bf16x2_to_float2(w.y);
+                    const uint2 w2 = *reinterpret_cast<const uint2 *>(vrow);
+                    vf[0] = bf16x2_to_float2(w2.x);
+                    vf[1] = bf16x2_to_float2(w2.y);
                 } else {
                     vf[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(vrow));
                 }
@@ -504,139 +487,102 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *
         if (lane == 0)
             mbar_arrive(&empty[stage]);
 
-        if (m.flags & kMetaLast) {
-            // ---- merge the four warps' partial states for this unit ----
+        if (bm.flags & kPieceLast) {
+            // ---- finish this worker's piece of the stream ----
             float l_tot = l_run + __shfl_xor_sync(FULL, l_run, 8);
             l_tot += __shfl_xor_sync(FULL, l_tot, 16);
-            if (slot == 0 && leader) {
-                sML[(warp * G + hsel) * 2 + 0] = m_run;
-                sML[(warp * G + hsel) * 2 + 1] = l_tot;
-            }
+            const bool complete = whole && (bm.flags & kStreamLast);
+            const size_t row0 = (size_t)bm.b * p.Hq + (size_t)bm.h * G;
+            float *part = p.ws_part +
+                          ((size_t)gw * 2 + ((bm.flags & kSlot1) ? 1 : 0)) * G * (D + 4);
 #pragma unroll
-            for (int g = 0; g < G; g++)
+            for (int g = 0; g < G; g++) {
+                const float mg = __shfl_sync(FULL, m_run, g << HSHIFT);
+                const float lg = __shfl_sync(FULL, l_tot, g << HSHIFT);
+                if (complete) {
+                    uint32_t pk[VP];
 #pragma unroll
-                for (int i = 0; i < VP; i++)
-                    *reinterpret_cast<float2 *>(sAcc + (warp * G + g) * D + lane * DPL + 2 * i) =
-                        acc[g][i];
-            named_barrier(1, kConsumerWarps * 32);
-            const int ct = warp * 32 + lane;
-            const bool single = (m.flags & kMetaSingle) != 0;
-            for (int idx = ct; idx < G * D; idx += kConsumerWarps * 32) {
-                const int g = idx / D;
-                const int d = idx - g * D;
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; w++)
-                    M = fmaxf(M, sML[(w * G + g) * 2]);
-                float Ls = 0.f, O = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; w++) {
-                    const float e = fast_exp2(sML[(w * G + g) * 2] - M);
-                    Ls += sML[(w * G + g) * 2 + 1] * e;
-                    O += sAcc[(w * G + g) * D + d] * e;
-                }
-                const size_t rowi = (size_t)m.b * p.Hq + (size_t)m.h * G + g;
-                if (single) {
-                    p.out[rowi * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(O / Ls));
+                    for (int i = 0; i < VP; i++) {
+                        const float x0 = lg > 0.f ? acc[g][i].x / lg : 0.f;
+                        const float x1 = lg > 0.f ? acc[g][i].y / lg : 0.f;
+                        pk[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x0)) |
+                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x1)) << 16);
+                    }
+                    uint16_t *o = p.out + (row0 + g) * D + lane * DPL;
+                    if constexpr (VP == 2)
+                        *reinterpret_cast<uint2 *>(o) = make_uint2(pk[0], pk[1]);
+                    else
+                        *reinterpret_cast<uint32_t *>(o) = pk[0];
                 } else {
-                    const size_t pi = rowi * p.S + m.c;
-                    p.ws_acc[pi * D + d] = O;
-                    if (d == 0) {
-                        p.ws_ml[pi * 2 + 0] = M;
-                        p.ws_ml[pi * 2 + 1] = Ls;
+                    float *pg = part + (size_t)g * (D + 4);
+                    if constexpr (VP == 2)
+                        *reinterpret_cast<float4 *>(pg + lane * DPL) =
+                            make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+                    else
+                        *reinterpret_cast<float2 *>(pg + lane * DPL) = acc[g][0];
+                    if (lane == 0) {
+                        pg[D] = mg;
+                        pg[D + 1] = lg;
                     }
                 }
             }
-            named_barrier(1, kConsumerWarps * 32);
-            m_run = -INFINITY;
-            l_run = 0.f;
-#pragma unroll
-            for (int g = 0; g < G; g++)
-#pragma unroll
-                for (int i = 0; i < VP; i++)
-                    acc[g][i] = make_float2(0.f, 0.f);
         }
-        if (++stage == STAGES) {
+        if (++stage == p.stages) {
             stage = 0;
             phase ^= 1;
         }
     }
 }
 
-// Build the CTA's unit map: per sequence its clamped length and number of
-// partitions, and sP[c] = number of (sequence, partition) pairs with
-// partition index < c, for c = 0..S.
-__device__ __forceinline__ void build_unit_map(const DecodeParams &p, uint8_t *smem,
-                                               const DecodeSmem &L)
+// Per-sequence clamped lengths and the exclusive prefix sum of their box
+// counts (boxes per KV head before sequence b), b = 0..B.
+__device__ __forceinline__ void build_prefix(const DecodeParams &p, int *pb, int *len, int *wsum)
 {
-    int *sP = reinterpret_cast<int *>(smem + L.prefix);
-    int *sH = reinterpret_cast<int *>(smem + L.hist);
-    int *sLen = reinterpret_cast<int *>(smem + L.lens);
-    uint16_t *sN = reinterpret_cast<uint16_t *>(smem + L.nch);
-    const int tid = threadIdx.x;
-    for (int i = tid; i <= p.S; i += blockDim.x)
-        sH[i] = 0;
-    __syncthreads();
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5;
     const int maxctx = p.MBS * p.bs;
+    const int per = (p.B + nt - 1) / nt;
+    const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
     bool bad = false;
-    for (int b = tid; b < p.B; b += blockDim.x) {
+    int local = 0;
+    for (int b = lo; b < hi; b++) {
         int n = __ldg(p.context_lens + b);
         if (n < 0 || n > maxctx) {
             bad = true;
             n = n < 0 ? 0 : maxctx;
         }
-        const int nc = (n + p.chunk - 1) / p.chunk;
-        sLen[b] = n;
-        sN[b] = (uint16_t)nc;
-        atomicAdd(&sH[nc], 1);
+        len[b] = n;
+        local += (n + kBox - 1) / kBox;
     }
     if (bad && blockIdx.x == 0)
         flag_error(p.err_flag, 0x4 /* PKV_FLAG_BAD_CONTEXT_LEN */);
-    __syncthreads();
-    if (tid < 32) {
-        const int lane = tid;
-        // sH[i] <- number of sequences with at least i partitions (suffix sum)
-        const int n = p.S + 1;
-        const int per = (n + 31) / 32;
-        const int lo = min(n, lane * per), hi = min(n, lo + per);
-        int tot = 0;
-        for (int i = lo; i < hi; i++)
-            tot += sH[i];
-        int incl = tot;  // sum over lanes >= this one
+    int incl = local;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int t = __shfl_down_sync(0xffffffffu, incl, off);
-            if (lane + off < 32)
-                incl += t;
-        }
-        int run = incl - tot;
-        for (int i = hi - 1; i >= lo; i--) {
-            run += sH[i];
-            sH[i] = run;
-        }
-        __syncwarp();
-        // sP[c] = sum_{c' < c} (sequences with more than c' partitions) = sum_{c'<c} sH[c'+1]
-        const int m = p.S;  // sP has S+1 entries; element c' contributes sH[c'+1]
-        const int per2 = (m + 31) / 32;
-        const int lo2 = min(m, lane * per2), hi2 = min(m, lo2 + per2);
-        int tot2 = 0;
-        for (int i = lo2; i < hi2; i++)
-            tot2 += sH[i + 1];
-        int inc2 = tot2;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, inc2, off);
-            if (lane >= off)
-                inc2 += t;
-        }
-        int run2 = inc2 - tot2;
-        for (int i = lo2; i < hi2; i++) {
-            sP[i] = run2;
-            run2 += sH[i + 1];
-        }
-        if (lane == 31)
-            sP[m] = inc2;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off)
+            incl += t;
     }
+    if (lane == 31)
+        wsum[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int w = 0; w < nt / 32; w++) {
+            const int t = wsum[w];
+            wsum[w] = run;
+            run += t;
+        }
+        wsum[nt / 32] = run;
+    }
+    __syncthreads();
+    int run = wsum[warp] + incl - local;
+    for (int b = lo; b < hi; b++) {
+        pb[b] = run;
+        run += (len[b] + kBox - 1) / kBox;
+    }
+    if (tid == 0)
+        pb[p.B] = wsum[nt / 32];
     __syncthreads();
 }
 
@@ -646,7 +592,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                         const __grid_constant__ CUtensorMap tmv, const DecodeParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const DecodeSmem L = decode_smem_layout(D, G, DecodeShape<D>::kStages, p.B, p.S);
+    const DecodeSmem L = decode_smem_layout(D, G, p.stages, p.B);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -654,23 +600,39 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (threadIdx.x == 0) {
         uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
         uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
-        for (int s = 0; s < DecodeShape<D>::kStages; s++) {
+        for (int s = 0; s < p.stages; s++) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], kWorkers);
         }
         fence_mbarrier_init();
     }
-    build_unit_map(p, smem, L);  // ends with __syncthreads()
+    int *pb = reinterpret_cast<int *>(smem + L.pb);
+    int *len = reinterpret_cast<int *>(smem + L.len);
+    build_prefix(p, pb, len, reinterpret_cast<int *>(smem + L.scan));  // ends with __syncthreads()
 
-    if (warp == kConsumerWarps)
-        decode_producer<D, G>(&tmk, &tmv, p, smem, L, lane);
-    else
+    const int T = pb[p.B] * p.Hkv;           // boxes over all streams
+    const int W = (int)gridDim.x * kWorkers; // workers
+    const int P = T > 0 ? (T + W - 1) / W : 1;
+
+    if (warp == kWorkers) {
+        decode_producer<D, G>(&tmk, &tmv, p, smem, L, lane, T, P);
+    } else {
+        if (blockIdx.x == 0) {
+            // Publish the box layout for the merge kernel (after the previous
+            // step's kernels, which may still read the workspace).
+            grid_dependency_wait();
+            for (int i = threadIdx.x; i <= p.B; i += kWorkers * 32)
+                p.ws_hdr[kWsHeaderInts + i] = pb[i];
+            if (threadIdx.x == 0) {
+                p.ws_hdr[0] = T;
+                p.ws_hdr[1] = P;
+                p.ws_hdr[2] = W;
+                p.ws_hdr[3] = p.B;
+            }
+        }
         decode_consumer<D, G>(p, smem, L, warp, lane);
+    }
 }
-
-template <int D, int G> struct DecodeLauncher {
-    static void *fn() { return reinterpret_cast<void *>(&paged_decode_kernel<D, G>); }
-};
 
 template <int D>
 inline cudaError_t launch_decode_dim(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,

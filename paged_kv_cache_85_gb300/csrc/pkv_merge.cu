@@ -1,15 +1,22 @@
-// Log-sum-exp merge of split-K partial results.
+// Log-sum-exp merge of the pieces of streams that straddle workers.
 //
-// A sequence whose context was cut into k > 1 partitions has, per query
-// head, k partial states (acc_c, m_c, l_c): acc_c = sum over the partition
-// of 2^(s_t - m_c) v_t, l_c = sum of 2^(s_t - m_c), with scores s in log2
-// units.  The full softmax result is
-//     M = max_c m_c,  out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
-// Sequences with one partition were written by the decode kernel directly;
-// sequences with context length 0 get zeros here.
+// The decode kernel cut the concatenated (sequence, KV head) box streams
+// into equal slices of P boxes, one per worker.  A stream [s, e) that lies in
+// one slice was finished by its worker and written to `out` directly.  A
+// stream spanning workers w0 = s / P .. w1 = (e - 1) / P left one partial
+// per worker, each (acc_i, m_i, l_i) per query head with
+// acc_i = sum over the piece of 2^(s_t - m_i) v_t and l_i = sum of
+// 2^(s_t - m_i) (scores in log2 units).  Worker w0's piece sits in its first
+// slot if the stream starts its slice, else in its second slot (the last
+// piece of that slice); every later worker's piece is its first.  The result
+// is
+//     M = max_i m_i,  out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.
+// Sequences with context length 0 get zeros here.
 //
 // One warp per (sequence, query head); each lane owns D/32 output columns.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "pkv_kernels.h"
 #include "pkv_ptx.cuh"
@@ -19,7 +26,7 @@ namespace pkv {
 constexpr int kMergeWarps = 4;
 
 template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_partitions_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_pieces_kernel(const DecodeParams p)
 {
     constexpr int DPL = D / 32;
     grid_launch_dependents();
@@ -28,52 +35,78 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_partitions_kernel(cons
     if (row >= (long long)p.B * p.Hq)
         return;
     const int b = (int)(row / p.Hq);
-    int n = __ldg(p.context_lens + b);
-    const int maxctx = p.MBS * p.bs;
-    n = n < 0 ? 0 : (n > maxctx ? maxctx : n);
-    const int nc = (n + p.chunk - 1) / p.chunk;
-    if (nc == 1)
-        return;
-    // Partials come from the decode kernel just before this one.
+    const int hq = (int)(row - (long long)b * p.Hq);
+    const int G = p.Hq / p.Hkv;
+    const int kvh = hq / G, g = hq - kvh * G;
+    // The box layout and the partials come from the decode kernel just before.
     grid_dependency_wait();
+    const int P = p.ws_hdr[1];
+    const int *pb = p.ws_hdr + kWsHeaderInts;
+    const int nb = pb[b + 1] - pb[b];
     uint16_t *o = p.out + row * D + lane * DPL;
-    if (nc == 0) {
+    if (nb == 0) {
 #pragma unroll
         for (int i = 0; i < DPL; i++)
             o[i] = 0;
         return;
     }
-    const float *ml = p.ws_ml + (size_t)row * p.S * 2;
+    const int s = pb[b] * p.Hkv + kvh * nb;
+    const int e = s + nb;
+    const int w0 = s / P, w1 = (e - 1) / P;
+    if (w0 == w1)
+        return;  // finished inside one worker
+    const int n = w1 - w0 + 1;
+    const int slot0 = (s == w0 * P) ? 0 : 1;
+    auto piece = [&](int i) -> const float * {
+        const int w = w0 + i;
+        const int slot = i == 0 ? slot0 : 0;
+        return p.ws_part + (((size_t)w * 2 + slot) * G + g) * (D + 4);
+    };
+
     float M = -INFINITY;
-    for (int c = lane; c < nc; c += 32)
-        M = fmaxf(M, ml[2 * c]);
+    for (int i = lane; i < n; i += 32)
+        M = fmaxf(M, piece(i)[D]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (M == -INFINITY) {  // no token of the stream could be read
+#pragma unroll
+        for (int i = 0; i < DPL; i++)
+            o[i] = 0;
+        return;
+    }
     float Ls = 0.f;
-    for (int c = lane; c < nc; c += 32)
-        Ls += ml[2 * c + 1] * fast_exp2(ml[2 * c] - M);
+    for (int i = lane; i < n; i += 32)
+        Ls += piece(i)[D + 1] * fast_exp2(piece(i)[D] - M);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
 
-    const float *a = p.ws_acc + (size_t)row * p.S * D + lane * DPL;
+    // Weighted sum of the partial outputs; 8 pieces' loads in flight at once.
+    using Vec = typename std::conditional<DPL == 4, float4, float2>::type;
     float acc[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; i++)
         acc[i] = 0.f;
-    for (int c = 0; c < nc; c++) {
-        const float w = fast_exp2(ml[2 * c] - M);
-        if constexpr (DPL == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(a + (size_t)c * D);
-            acc[0] += w * x.x;
-            acc[1] += w * x.y;
-            acc[2] += w * x.z;
-            acc[3] += w * x.w;
-        } else {
-            const float2 x = *reinterpret_cast<const float2 *>(a + (size_t)c * D);
-            acc[0] += w * x.x;
-            acc[1] += w * x.y;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const int m = min(32, n - c0);
+        const float wl = lane < m ? fast_exp2(piece(c0 + lane)[D] - M) : 0.f;
+        for (int j0 = 0; j0 < m; j0 += 8) {
+            Vec x[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                if (j0 + j < m)
+                    x[j] = *reinterpret_cast<const Vec *>(piece(c0 + j0 + j) + lane * DPL);
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const float w = __shfl_sync(0xffffffffu, wl, (j0 + j) & 31);
+                if (j0 + j < m) {
+                    const float *xv = reinterpret_cast<const float *>(&x[j]);
+#pragma unroll
+                    for (int i = 0; i < DPL; i++)
+                        acc[i] += w * xv[i];
+                }
+            }
         }
     }
 #pragma unroll
@@ -81,8 +114,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_partitions_kernel(cons
         o[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i] / Ls));
 }
 
-cudaError_t launch_merge(int D, const DecodeParams &p, cudaStream_t stream)
+cudaError_t launch_merge(int D, int G, const DecodeParams &p, cudaStream_t stream)
 {
+    (void)G;
     const long long rows = (long long)p.B * p.Hq;
     if (rows == 0)
         return cudaSuccess;
@@ -96,9 +130,9 @@ cudaError_t launch_merge(int D, const DecodeParams &p, cudaStream_t stream)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (D == 128)
-        return cudaLaunchKernelEx(&cfg, merge_partitions_kernel<128>, p);
+        return cudaLaunchKernelEx(&cfg, merge_pieces_kernel<128>, p);
     if (D == 64)
-        return cudaLaunchKernelEx(&cfg, merge_partitions_kernel<64>, p);
+        return cudaLaunchKernelEx(&cfg, merge_pieces_kernel<64>, p);
     return cudaErrorInvalidValue;
 }
 

@@ -45,12 +45,16 @@ def test_host_only_entry_points(cuda_lib_path):
     assert lib.pkv_version() >= 100
     f = lib.pkv_decode_workspace_bytes
     f.restype = ctypes.c_size_t
-    f.argtypes = [ctypes.c_int] * 6
-    # one partition per sequence -> no partials needed
-    assert f(4, 4, 64, 19, 16, 1) == 0
-    # 4096-token contexts in 256-token partitions: 16 partials of (D + 2) floats per row
-    assert f(64, 16, 128, 16, 256, 0) == 64 * 16 * 16 * 130 * 4
-    assert f(-1, 4, 64, 19, 16, 0) == 0
+    f.argtypes = [ctypes.c_int] * 7
+    hdr = lambda B: (4 + B + 1) * 4 + (-(4 + B + 1) * 4) % 256
+    # 4 seqs x 2 KV heads x 19 boxes = 152 boxes -> 19 CTAs of 8 workers, 2 slots of 2 x (64 + 4) floats
+    assert f(4, 4, 2, 64, 19, 16, 0) == hdr(4) + 19 * 8 * 2 * 2 * 68 * 4
+    # large problems: capped at 256 CTAs; max_ctas caps further
+    assert f(64, 16, 8, 128, 16, 256, 0) == hdr(64) + 256 * 8 * 2 * 2 * 132 * 4
+    assert f(64, 16, 8, 128, 16, 256, 10) == hdr(64) + 10 * 8 * 2 * 2 * 132 * 4
+    assert f(-1, 4, 2, 64, 19, 16, 0) == 0
+    assert f(0, 4, 2, 64, 19, 16, 0) == 0
+    assert f(4, 6, 4, 64, 19, 16, 0) == 0  # Hq not a multiple of Hkv
     lib.pkv_status_string.restype = ctypes.c_char_p
     assert lib.pkv_status_string(3) == b"PKV_ERR_WORKSPACE"
 

@@ -49,11 +49,11 @@ def to_dev(w):
     )
 
 
-def run_step(pkv, w, d, num_splits=0, err=None):
+def run_step(pkv, w, d, max_ctas=0, err=None):
     pkv.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slots"], err_flag=err)
     out = torch.empty_like(d["q"])
     pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["tables"], d["lens"], w.scale, out,
-                          num_splits=num_splits, err_flag=err)
+                          max_ctas=max_ctas, err_flag=err)
     torch.cuda.synchronize()
     return out
 
@@ -98,18 +98,19 @@ def test_config_store_bitexact_and_decode_parity(pkv, idx):
     compare(out, ref, w.name)
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 5, 19, 0])
-def test_split_count_invariance_tiny(pkv, splits):
+@pytest.mark.parametrize("ctas", [1, 2, 3, 5, 7, 0])
+def test_grid_size_invariance_tiny(pkv, ctas):
+    """Fewer CTAs move the slice boundaries (and so the merges) elsewhere."""
     w, (kc, vc, ref) = config(0)
     d = to_dev(w)
-    out = run_step(pkv, w, d, num_splits=splits)
-    compare(out, ref, f"splits={splits}")
+    out = run_step(pkv, w, d, max_ctas=ctas)
+    compare(out, ref, f"max_ctas={ctas}")
 
 
-def test_split_counts_agree_qwen3_shape(pkv):
+def test_grid_sizes_agree_qwen3_shape(pkv):
     w, (kc, vc, ref) = config(1)
     d = to_dev(w)
-    outs = [run_step(pkv, w, d, num_splits=s) for s in (1, 4, 16, 0)]
+    outs = [run_step(pkv, w, d, max_ctas=s) for s in (1, 13, 77, 0)]
     for o in outs:
         compare(o, ref)
     a = wl.bf16_bits_to_f32(bits_host(outs[0]))
@@ -133,9 +134,9 @@ def test_group_dim_block_variants(pkv, G, D, bs):
     w = _random_problem(rng, len(lens), G * Hkv, Hkv, D, bs, lens)
     kc, vc, ref = oracle_step(w)
     d = to_dev(w)
-    for splits in (0, 1, 3):
-        out = run_step(pkv, w, d, num_splits=splits)
-        compare(out, ref, f"G={G} D={D} bs={bs} splits={splits}")
+    for ctas in (0, 1, 3):
+        out = run_step(pkv, w, d, max_ctas=ctas)
+        compare(out, ref, f"G={G} D={D} bs={bs} max_ctas={ctas}")
 
 
 def test_context_len_one_returns_v_bitexact(pkv):
@@ -174,7 +175,7 @@ def test_nan_in_unread_slots_changes_nothing(pkv):
     lens = [1, 17, 40, 300, 33]
     w = _random_problem(rng, 5, 8, 2, 128, 16, lens)
     d = to_dev(w)
-    clean = bits_host(run_step(pkv, w, d, num_splits=2))
+    clean = bits_host(run_step(pkv, w, d, max_ctas=2))
     kc, vc = w.k_cache.copy(), w.v_cache.copy()
     # store first on the host so poisoning leaves the new tokens intact
     kc, vc, _ = oracle.store_kvcache(w.k_new, w.v_new, kc, vc, w.slot_mapping)
@@ -182,7 +183,7 @@ def test_nan_in_unread_slots_changes_nothing(pkv):
     d2 = to_dev(w)
     d2["k_cache"], d2["v_cache"] = bf16_dev(kc), bf16_dev(vc)
     d2["slots"] = torch.full_like(d2["slots"], -1)
-    out = bits_host(run_step(pkv, w, d2, num_splits=2))
+    out = bits_host(run_step(pkv, w, d2, max_ctas=2))
     assert np.isfinite(wl.bf16_bits_to_f32(out)).all()
     np.testing.assert_array_equal(out, clean)
 
@@ -208,7 +209,7 @@ def test_zero_context_gives_zeros(pkv):
     w = _random_problem(rng, 3, 4, 2, 64, 16, [5, 9, 300])
     d = to_dev(w)
     d["lens"] = torch.tensor([0, 9, 0], dtype=torch.int32, device="cuda")
-    out = bits_host(run_step(pkv, w, d, num_splits=4))
+    out = bits_host(run_step(pkv, w, d, max_ctas=4))
     assert (out[0] == 0).all() and (out[2] == 0).all()
     assert (out[1] != 0).any()
 
@@ -247,7 +248,7 @@ def test_workspace_too_small_is_rejected(pkv):
     small = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(pkv.PkvError):
         pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["tables"], d["lens"], w.scale,
-                              out, num_splits=4, workspace=small)
+                              out, workspace=small)
 
 
 def test_cuda_graph_capture_and_replay(pkv):
@@ -277,6 +278,6 @@ def test_back_to_back_steps_on_one_stream(pkv):
     for _ in range(20):
         pkv.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slots"])
         pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["tables"], d["lens"], w.scale,
-                              out, num_splits=3)
+                              out, max_ctas=3)
     torch.cuda.synchronize()
     compare(out, ref, "20 steps")
