@@ -163,6 +163,12 @@ def reduce_max(value: float, dist, device=None) -> float:
     return float(t.item())
 
 
+def job_throughput(bytes_per_rank_step: int, world: int, ms_step_max: float) -> float:
+    """Whole-job GB/s: every rank moves the same bytes per step; the job's step
+    time is the slowest rank's."""
+    return world * bytes_per_rank_step / (ms_step_max * 1e-3) / 1e9
+
+
 def barrier(dist, device=None):
     if dist is not None:
         if device is not None and device.type == "cuda":
@@ -174,13 +180,16 @@ def barrier(dist, device=None):
 # ----------------------------------------------------------- CPU oracle leg
 
 
-def oracle_sample(w, seqs):
-    """Run the oracle's store + decode on sequences `seqs` of the step; return bytes moved."""
+def oracle_sample(w, seqs, kc, vc):
+    """Run the oracle's store + decode on sequences `seqs` of the step; return bytes moved.
+
+    `kc`, `vc` are the oracle's own copies of the caches (the store writes
+    them in place, as the GPU path does).
+    """
     import oracle
 
     sel = np.asarray(seqs)
-    slots = w.slot_mapping[sel]
-    kc, vc, _ = oracle.store_kvcache(w.k_new[sel], w.v_new[sel], w.k_cache, w.v_cache, slots)
+    oracle.store_kvcache_(w.k_new[sel], w.v_new[sel], kc, vc, w.slot_mapping[sel])
     pairs = np.array([(b, h) for b in sel for h in range(w.Hq)], np.int32)
     oracle.paged_attn_decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, pairs=pairs)
     return sample_bytes(w, sel)
@@ -198,12 +207,13 @@ def sample_bytes(w, sel):
 
 def time_oracle(w, budget_s: float):
     """Time the oracle on a bounded sample (a prefix of the sequences) of the step."""
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
     t0 = time.perf_counter()
-    oracle_sample(w, [0])  # also compiles / loads the oracle
+    oracle_sample(w, [0], kc, vc)  # also compiles / loads the oracle
     one = max(time.perf_counter() - t0, 1e-4)
     m = int(max(1, min(w.B, budget_s / one)))
     t0 = time.perf_counter()
-    nbytes = oracle_sample(w, list(range(m)))
+    nbytes = oracle_sample(w, list(range(m)), kc, vc)
     dt = time.perf_counter() - t0
     return {
         "value": nbytes / dt / 1e9,
@@ -322,7 +332,7 @@ def run_ours(args):
     ms_attn = reduce_max(ms_attn, dist, dev)
     ms_e2e = reduce_max(ms_e2e, dist, dev)
     ms_step = ms_total / args.steps
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = job_throughput(step_bytes, world, ms_step)
     peak, peak_src = load_peaks()
     achieved = w.decode_bytes() / (ms_attn * 1e-3) / 1e9
 
@@ -378,7 +388,7 @@ def run_ours(args):
             "us_per_launch": round(ms_attn * 1e3, 2),
         },
         "e2e": {
-            "value": round(world * step_bytes / (ms_e2e * 1e-3) / 1e9, 2),
+            "value": round(job_throughput(step_bytes, world, ms_e2e), 2),
             "unit": "GB/s",
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
@@ -407,18 +417,19 @@ def run_reference(args):
     from paged_kv_cache_85_gb300 import workload as wl
 
     w = wl.config_workload(args.config)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
     t0 = time.perf_counter()
-    oracle_sample(w, [0])
+    oracle_sample(w, [0], kc, vc)
     one = max(time.perf_counter() - t0, 1e-4)
     budget = 150.0 / max(1, args.steps + args.warmup)
     m = int(max(1, min(w.B, budget / one)))
     seqs = list(range(m))
     for _ in range(args.warmup):
-        oracle_sample(w, seqs)
+        oracle_sample(w, seqs, kc, vc)
     t0 = time.perf_counter()
     nbytes = 0
     for _ in range(args.steps):
-        nbytes += oracle_sample(w, seqs)
+        nbytes += oracle_sample(w, seqs, kc, vc)
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9
     sample = (f"each step: store+decode of the first {m} of {w.B} sequences (all heads), "

@@ -90,6 +90,26 @@ def store_kvcache(k, v, k_cache, v_cache, slot_mapping):
     return kc, vc, int(bad)
 
 
+def store_kvcache_(k, v, k_cache, v_cache, slot_mapping) -> int:
+    """In-place variant of store_kvcache: writes into ``k_cache`` / ``v_cache``.
+
+    The caches must be C-contiguous uint16 arrays.  Returns the number of
+    out-of-range slots (skipped).
+    """
+    lib = _load()
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    for c in (k_cache, v_cache):
+        if c.dtype != np.uint16 or not c.flags["C_CONTIGUOUS"] or not c.flags["WRITEABLE"]:
+            raise ValueError("caches must be writeable C-contiguous uint16 arrays")
+    NB, bs, Hkv, D = k_cache.shape
+    N = slots.shape[0]
+    assert k.shape == (N, Hkv, D) and v.shape == (N, Hkv, D) and v_cache.shape == k_cache.shape
+    return int(lib.oracle_store_kvcache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(slots), N, Hkv, D, NB, bs))
+
+
 def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, pairs=None):
     """fp64 decode attention.
 

@@ -304,3 +304,19 @@ def test_invalid_table_entry_reported():
     t2[1, 1] = 99  # past NB
     out = oracle.paged_attn_decode(q, kc, vc, t2, ctx, 0.25)
     assert (out[1] == 0).all()
+
+
+def test_inplace_store_matches_functional_store():
+    rng = np.random.default_rng(15)
+    NB, bs, Hkv, D, N = 5, 16, 2, 8, 9
+    kc0 = rng.integers(0, 1 << 16, (NB, bs, Hkv, D), dtype=np.uint16)
+    vc0 = rng.integers(0, 1 << 16, (NB, bs, Hkv, D), dtype=np.uint16)
+    k = rng.integers(0, 1 << 16, (N, Hkv, D), dtype=np.uint16)
+    v = rng.integers(0, 1 << 16, (N, Hkv, D), dtype=np.uint16)
+    slots = rng.choice(NB * bs, size=N, replace=False).astype(np.int64)
+    slots[3] = -1
+    kc, vc, bad = oracle.store_kvcache(k, v, kc0, vc0, slots)
+    kc2, vc2 = kc0.copy(), vc0.copy()
+    assert oracle.store_kvcache_(k, v, kc2, vc2, slots) == bad == 0
+    np.testing.assert_array_equal(kc, kc2)
+    np.testing.assert_array_equal(vc, vc2)
