@@ -154,6 +154,38 @@ pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void 
                                  size_t workspace_bytes, int max_ctas, int32_t *err_flag,
                                  void *stream);
 
+/*
+ * pkv_paged_attn_decode_noalloc - pkv_paged_attn_decode without a workspace
+ * argument, for callers that cannot allocate device memory.
+ *
+ * (No counterpart in the pages: this is an interface convenience.)  Some
+ * callers must not call cudaMalloc or any allocating routine when they run
+ * decode attention, for instance code running inside a custom allocator or
+ * memory pool, or a runtime that only owns the step's input and output
+ * buffers.  This call computes exactly what pkv_paged_attn_decode computes
+ * (same arguments and results, within rounding) but keeps its scratch in a
+ * fixed device array of PKV_NOALLOC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library's device code holds until the process
+ * exits.  It allocates nothing.  The grid is capped so the scratch fits;
+ * sizes that do not fit even one CTA (huge B with large G and D) return
+ * PKV_ERR_WORKSPACE with a message, and pkv_paged_attn_decode with a
+ * caller workspace remains available for them.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it: make that
+ * first call before any CUDA stream capture.  All calls share the one array
+ * and it keeps the last call's contents (nothing in it needs to start at
+ * zero).  Calls that overlap on the GPU race on it: serialise them (one
+ * stream per device, or events between streams).
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+pkv_status pkv_paged_attn_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *block_tables, int MBS,
+                                         const int32_t *context_lens, int B, int Hq, int Hkv,
+                                         int D, int64_t NB, int bs, float scale, void *out,
+                                         int32_t *err_flag, void *stream);
+
 /* Message describing the last non-OK status returned on this host thread. */
 const char *pkv_last_error(void);
 

@@ -192,6 +192,14 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
 
 } // namespace
 
+namespace pkv {
+// Record a message for pkv_last_error() from another translation unit.
+pkv_status report_error(pkv_status s, const char *msg)
+{
+    return fail(s, "%s", msg);
+}
+} // namespace pkv
+
 extern "C" {
 
 const char *pkv_last_error(void) { return g_last_error; }
