@@ -16,12 +16,33 @@
 #include "pkv_kernels.h"
 
 namespace pkv {
-cudaError_t launch_decode_d64(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                              const DecodeParams &p, int grid, size_t smem, cudaStream_t stream);
-cudaError_t launch_decode_d128(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                               const DecodeParams &p, int grid, size_t smem, cudaStream_t stream);
-const void *decode_kernel_d64(int G);
-const void *decode_kernel_d128(int G);
+#define PKV_DECLARE_SHAPE(D, NW)                                                                  \
+    cudaError_t launch_decode_d##D##_w##NW(int G, const CUtensorMap *tmk, const CUtensorMap *tmv, \
+                                           const DecodeParams &p, int grid, size_t smem,          \
+                                           cudaStream_t stream);                                  \
+    const void *decode_kernel_d##D##_w##NW(int G);
+PKV_DECLARE_SHAPE(64, 4)
+PKV_DECLARE_SHAPE(64, 8)
+PKV_DECLARE_SHAPE(128, 4)
+PKV_DECLARE_SHAPE(128, 8)
+#undef PKV_DECLARE_SHAPE
+
+const void *decode_kernel(int D, int NW, int G)
+{
+    if (D == 128)
+        return NW == kPairWorkers ? decode_kernel_d128_w4(G) : decode_kernel_d128_w8(G);
+    return NW == kPairWorkers ? decode_kernel_d64_w4(G) : decode_kernel_d64_w8(G);
+}
+
+cudaError_t launch_decode(int D, int NW, int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                          const DecodeParams &p, int grid, size_t smem, cudaStream_t stream)
+{
+    if (D == 128)
+        return NW == kPairWorkers ? launch_decode_d128_w4(G, tmk, tmv, p, grid, smem, stream)
+                                  : launch_decode_d128_w8(G, tmk, tmv, p, grid, smem, stream);
+    return NW == kPairWorkers ? launch_decode_d64_w4(G, tmk, tmv, p, grid, smem, stream)
+                              : launch_decode_d64_w8(G, tmk, tmv, p, grid, smem, stream);
+}
 } // namespace pkv
 
 namespace {
@@ -42,13 +63,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool group_supported(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kMaxDynSmem = 227 * 1024;
-constexpr int kMaxGrid = 256;  // CTAs of one decode launch (one per SM)
+constexpr long long kMaxWorkersTotal = 2048;  // workers of one decode launch (256 SMs x 8)
+using pkv::kMaxDynSmem;
 
 struct DeviceState {
     bool ready = false;
     int sms = 0;
-    bool smem_set[2][9] = {};  // [D == 128][G]
+    bool smem_set[2][2][9] = {};  // [D == 128][NW == 8][G]
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -110,7 +131,7 @@ pkv_status make_cache_map(CUtensorMap *map, const void *cache, long long tokens,
 // workspace layout.  The workspace query and the launch share it, so they
 // always agree.
 struct DecodePlan {
-    int G = 0, stages = 0, grid = 0;
+    int G = 0, NW = 0, stages = 0, grid = 0;
     size_t smem = 0, hdr_bytes = 0, ws_bytes = 0;
     const void *kernel = nullptr;
 };
@@ -138,25 +159,34 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
     const long long box_max = (long long)B * Hkv * (((long long)MBS * bs + pkv::kBox - 1) / pkv::kBox);
     if (box_max >= 0x7fffffffLL)
         return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: B*Hkv*MBS*bs/16 must be < 2^31");
-    const int stages = pkv::decode_stages_for(D, G, B, kMaxDynSmem);
+    // Prefer two 4-worker CTAs per SM; fall back to one 8-worker CTA per SM
+    // when two do not fit (large B, or G = 8 with D = 128).
+    const size_t pair_smem = pkv::kSmemPerSm / 2 - pkv::kSmemReserve;
+    int NW = pkv::kPairWorkers;
+    int stages = pkv::decode_stages_for(D, G, NW, B, pkv::kPairStages, pair_smem);
+    if (stages < pkv::kPairStages) {
+        NW = pkv::kWideWorkers;
+        stages = pkv::decode_stages_for(D, G, NW, B, pkv::kMaxStages, kMaxDynSmem);
+    }
     if (stages == 0)
         return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: B=%d does not fit shared memory", B);
     // The workspace is sized for the largest grid the launch may use, which
-    // depends only on the arguments: one CTA per SM, at most kMaxGrid CTAs,
-    // and no more than the boxes can keep busy.
-    long long grid_cap = (box_max + pkv::kWorkers - 1) / pkv::kWorkers;
-    if (grid_cap > kMaxGrid)
-        grid_cap = kMaxGrid;
+    // depends only on the arguments: no more CTAs than the boxes can keep
+    // busy, at most kMaxWorkersTotal workers, and at most max_ctas.
+    long long grid_cap = (box_max + NW - 1) / NW;
+    if (grid_cap > kMaxWorkersTotal / NW)
+        grid_cap = kMaxWorkersTotal / NW;
     if (max_ctas > 0 && grid_cap > max_ctas)
         grid_cap = max_ctas;
     if (grid_cap < 1)
         grid_cap = 1;
     plan->G = G;
+    plan->NW = NW;
     plan->stages = stages;
-    plan->smem = pkv::decode_smem_layout(D, G, stages, B).total;
+    plan->smem = pkv::decode_smem_layout(D, G, NW, stages, B).total;
     plan->hdr_bytes = pkv::align_up((size_t)(pkv::kWsHeaderInts + B + 1) * 4, 256);
     plan->ws_bytes = plan->hdr_bytes +
-                     (size_t)grid_cap * pkv::kWorkers * 2 * G * (size_t)(D + 4) * sizeof(float);
+                     (size_t)grid_cap * NW * 2 * G * (size_t)(D + 4) * sizeof(float);
     plan->grid = (int)grid_cap;
     if (!with_device)
         return PKV_OK;
@@ -164,10 +194,10 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
     pkv_status ps = device_state(&st);
     if (ps != PKV_OK)
         return ps;
-    const void *kfn = D == 128 ? pkv::decode_kernel_d128(G) : pkv::decode_kernel_d64(G);
+    const void *kfn = pkv::decode_kernel(D, NW, G);
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        bool &set = st->smem_set[D == 128][G];
+        bool &set = st->smem_set[D == 128][NW == pkv::kWideWorkers][G];
         if (!set) {
             cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)kMaxDynSmem);
@@ -178,7 +208,7 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
     }
     int occ = 0;
     cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kfn, pkv::kDecodeThreads, plan->smem);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kfn, (NW + 1) * 32, plan->smem);
     if (e != cudaSuccess)
         return fail(PKV_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
     if (occ < 1)
@@ -313,8 +343,7 @@ pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void 
     p.scale_log2 = scale * 1.4426950408889634f;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = D == 128 ? pkv::launch_decode_d128(plan.G, &tmk, &tmv, p, plan.grid, plan.smem, s)
-                             : pkv::launch_decode_d64(plan.G, &tmk, &tmv, p, plan.grid, plan.smem, s);
+    cudaError_t e = pkv::launch_decode(D, plan.NW, plan.G, &tmk, &tmv, p, plan.grid, plan.smem, s);
     if (e != cudaSuccess)
         return fail(PKV_ERR_CUDA, "paged_attn_decode launch: %s", cudaGetErrorString(e));
     e = pkv::launch_merge(D, plan.G, p, s);

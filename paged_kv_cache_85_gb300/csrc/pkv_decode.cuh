@@ -70,37 +70,37 @@ struct DecodeSmem {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int stages, int B)
+__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int NW, int stages, int B)
 {
     DecodeSmem L;
     size_t o = 0;
-    L.kv = o;  // per stage: K boxes [kWorkers][16][D], then V boxes [kWorkers][16][D]
-    o += (size_t)stages * 2 * kWorkers * kBox * D * 2;
+    L.kv = o;  // per stage: K boxes [NW][16][D], then V boxes [NW][16][D]
+    o += (size_t)stages * 2 * NW * kBox * D * 2;
     L.q = o;  // per stage and worker: G query rows
-    o = align_up(o + (size_t)stages * kWorkers * G * D * 2, 16);
+    o = align_up(o + (size_t)stages * NW * G * D * 2, 16);
     L.pbuf = o;  // per worker: probabilities [16 tokens][G] as (p, p) pairs
-    o = align_up(o + (size_t)kWorkers * kBox * G * 8, 16);
+    o = align_up(o + (size_t)NW * kBox * G * 8, 16);
     L.full = o;
     o += (size_t)stages * 8;
     L.empty = o;
     o += (size_t)stages * 8;
     L.meta = o = align_up(o, 16);
-    o += (size_t)stages * kWorkers * sizeof(BoxMeta);
+    o += (size_t)stages * NW * sizeof(BoxMeta);
     L.pb = o;  // boxes per KV head before sequence b, b = 0..B
     o = align_up(o + (size_t)(B + 1) * 4, 16);
     L.len = o;  // clamped context length per sequence
     o = align_up(o + (size_t)B * 4, 16);
     L.scan = o;  // per-warp partial sums of the prefix scan
-    o = align_up(o + (size_t)(kDecodeThreads / 32 + 1) * 4, 16);
+    o = align_up(o + (size_t)(NW + 2) * 4, 16);
     L.total = o;
     return L;
 }
 
-// Deepest pipeline (2..4 stages) whose shared memory fits one CTA per SM.
-inline int decode_stages_for(int D, int G, int B, size_t max_smem)
+// Deepest pipeline (2..max_stages) whose shared memory fits max_smem.
+inline int decode_stages_for(int D, int G, int NW, int B, int max_stages, size_t max_smem)
 {
-    for (int s = kMaxStages; s >= kMinStages; s--)
-        if (decode_smem_layout(D, G, s, B).total <= max_smem)
+    for (int s = max_stages; s >= kMinStages; s--)
+        if (decode_smem_layout(D, G, NW, s, B).total <= max_smem)
             return s;
     return 0;
 }
@@ -188,13 +188,13 @@ __device__ __forceinline__ int box_block(const DecodeParams &p, int b, int j)
     return __ldg(p.block_tables + (size_t)b * p.MBS + (j * kBox) / p.bs);
 }
 
-// Producer warp: lane w < kWorkers runs worker w of this CTA.  Each lane
+// Producer warp: lane w < NW runs worker w of this CTA.  Each lane
 // walks its own slice with two cursors: the issue cursor, and a look-ahead
 // cursor kLookahead boxes further on whose block ids are loaded into a small
 // register queue, so a copy never waits on a block-table read.  Per stage
 // every lane writes its worker's box descriptor and issues its own TMA
 // copies; lane 0 arms the stage's mbarrier with the summed byte count.
-template <int D, int G>
+template <int D, int G, int NW>
 __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CUtensorMap *tmv,
                                                 const DecodeParams &p, uint8_t *smem,
                                                 const DecodeSmem &L, int lane, int T, int P)
@@ -211,8 +211,8 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
         prefetch_tensormap(tmk);
         prefetch_tensormap(tmv);
     }
-    const bool worker = lane < kWorkers;
-    const long long s0 = ((long long)blockIdx.x * kWorkers + lane) * P;
+    const bool worker = lane < NW;
+    const long long s0 = ((long long)blockIdx.x * NW + lane) * P;
     const int start = worker ? (int)(s0 < T ? s0 : T) : T;
     const int end = worker ? (int)(s0 + P < T ? s0 + P : T) : T;
     int pos = start;
@@ -265,7 +265,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
                 first_done = true;
             bytes = (loaded ? 2u * kBoxBytes : 0u) + (pf ? (uint32_t)(G * D * 2) : 0u);
             row = loaded ? blk * p.bs + tok0 % p.bs : 0;
-            BoxMeta &m = meta[stage * kWorkers + lane];
+            BoxMeta &m = meta[stage * NW + lane];
             m.b = b;
             m.h = h;
             m.tok0 = tok0;
@@ -285,7 +285,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
             }
             ++lpos;
         } else if (worker) {
-            meta[stage * kWorkers + lane].flags = 0;
+            meta[stage * NW + lane].flags = 0;
         }
         bytes = __reduce_add_sync(FULL, bytes);
         __syncwarp();
@@ -293,12 +293,12 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
             mbar_arrive_expect_tx(&full[stage], bytes);
         __syncwarp();
         if (flags & kPieceFirst)
-            bulk_load(smem + L.q + ((size_t)stage * kWorkers + lane) * G * D * 2,
+            bulk_load(smem + L.q + ((size_t)stage * NW + lane) * G * D * 2,
                       p.q + ((size_t)b * p.Hq + (size_t)h * G) * D, G * D * 2, &full[stage]);
         if (flags & kBoxLoaded) {
-            uint8_t *kd = smem + L.kv + ((size_t)stage * 2 * kWorkers + lane) * kBoxBytes;
+            uint8_t *kd = smem + L.kv + ((size_t)stage * 2 * NW + lane) * kBoxBytes;
             tma_load_3d(kd, tmk, 0, h, row, &full[stage]);
-            tma_load_3d(kd + (size_t)kWorkers * kBoxBytes, tmv, 0, h, row, &full[stage]);
+            tma_load_3d(kd + (size_t)NW * kBoxBytes, tmv, 0, h, row, &full[stage]);
         }
         if (++stage == p.stages) {
             stage = 0;
@@ -312,13 +312,13 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
         return;
     }
     if (worker)
-        meta[stage * kWorkers + lane].flags = kStageStop;
+        meta[stage * NW + lane].flags = kStageStop;
     __syncwarp();
     if (lane == 0)
         mbar_arrive(&full[stage]);
 }
 
-template <int D, int G>
+template <int D, int G, int NW>
 __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *smem,
                                                 const DecodeSmem &L, int warp, int lane)
 {
@@ -340,7 +340,7 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *
     const int slot = lane >> 3;    // which of 4 tokens this lane scores per step
     const int hsel = r >> HSHIFT;  // head of this lane's score after the reduction
     const bool leader = (r & ((1 << HSHIFT) - 1)) == 0;
-    const int gw = blockIdx.x * kWorkers + warp;
+    const int gw = blockIdx.x * NW + warp;
 
     float2 qv[G][EP];
     float2 acc[G][VP];
@@ -364,11 +364,11 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *
                 flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
             return;
         }
-        const BoxMeta bm = meta[stage * kWorkers + warp];
+        const BoxMeta bm = meta[stage * NW + warp];
         if (bm.flags & kStageStop)
             break;
         if (bm.flags & kPieceFirst) {
-            const uint8_t *qs = smem + L.q + ((size_t)stage * kWorkers + warp) * G * D * 2;
+            const uint8_t *qs = smem + L.q + ((size_t)stage * NW + warp) * G * D * 2;
             const float2 sc = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
             for (int g = 0; g < G; g++)
@@ -392,8 +392,8 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *
         }
         const int nvw = (bm.flags & kBoxLoaded) ? bm.nvalid : 0;
         if (nvw > 0) {
-            const uint8_t *Ks = smem + L.kv + ((size_t)stage * 2 * kWorkers + warp) * kBoxBytes;
-            const uint8_t *Vs = Ks + (size_t)kWorkers * kBoxBytes;
+            const uint8_t *Ks = smem + L.kv + ((size_t)stage * 2 * NW + warp) * kBoxBytes;
+            const uint8_t *Vs = Ks + (size_t)NW * kBoxBytes;
             // ---- scores for the box's 16 tokens (4 per step) ----
             float sv[4];
 #pragma unroll
@@ -586,13 +586,13 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int *pb, int
     __syncthreads();
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kDecodeThreads, 1)
+template <int D, int G, int NW>
+__global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? 2 : 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const DecodeSmem L = decode_smem_layout(D, G, p.stages, p.B);
+    const DecodeSmem L = decode_smem_layout(D, G, NW, p.stages, p.B);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
         for (int s = 0; s < p.stages; s++) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kWorkers);
+            mbar_init(&empty[s], NW);
         }
         fence_mbarrier_init();
     }
@@ -611,17 +611,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     build_prefix(p, pb, len, reinterpret_cast<int *>(smem + L.scan));  // ends with __syncthreads()
 
     const int T = pb[p.B] * p.Hkv;           // boxes over all streams
-    const int W = (int)gridDim.x * kWorkers; // workers
+    const int W = (int)gridDim.x * NW; // workers
     const int P = T > 0 ? (T + W - 1) / W : 1;
 
-    if (warp == kWorkers) {
-        decode_producer<D, G>(&tmk, &tmv, p, smem, L, lane, T, P);
+    if (warp == NW) {
+        decode_producer<D, G, NW>(&tmk, &tmv, p, smem, L, lane, T, P);
     } else {
         if (blockIdx.x == 0) {
             // Publish the box layout for the merge kernel (after the previous
             // step's kernels, which may still read the workspace).
             grid_dependency_wait();
-            for (int i = threadIdx.x; i <= p.B; i += kWorkers * 32)
+            for (int i = threadIdx.x; i <= p.B; i += NW * 32)
                 p.ws_hdr[kWsHeaderInts + i] = pb[i];
             if (threadIdx.x == 0) {
                 p.ws_hdr[0] = T;
@@ -630,41 +630,41 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 p.ws_hdr[3] = p.B;
             }
         }
-        decode_consumer<D, G>(p, smem, L, warp, lane);
+        decode_consumer<D, G, NW>(p, smem, L, warp, lane);
     }
 }
 
-template <int D>
-inline cudaError_t launch_decode_dim(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                                     const DecodeParams &p, int grid, size_t smem,
-                                     cudaStream_t stream)
+template <int D, int NW>
+inline cudaError_t launch_decode_shape(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                                       const DecodeParams &p, int grid, size_t smem,
+                                       cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.blockDim = dim3((NW + 1) * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     switch (G) {
-    case 1: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 1>, *tmk, *tmv, p);
-    case 2: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 2>, *tmk, *tmv, p);
-    case 4: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 4>, *tmk, *tmv, p);
-    case 8: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 8>, *tmk, *tmv, p);
+    case 1: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 1, NW>, *tmk, *tmv, p);
+    case 2: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 2, NW>, *tmk, *tmv, p);
+    case 4: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 4, NW>, *tmk, *tmv, p);
+    case 8: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 8, NW>, *tmk, *tmv, p);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int D> inline const void *decode_kernel_ptr(int G)
+template <int D, int NW> inline const void *decode_kernel_shape(int G)
 {
     switch (G) {
-    case 1: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 1>);
-    case 2: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 2>);
-    case 4: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 4>);
-    case 8: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 8>);
+    case 1: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 1, NW>);
+    case 2: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 2, NW>);
+    case 4: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 4, NW>);
+    case 8: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 8, NW>);
     default: return nullptr;
     }
 }

@@ -13,10 +13,18 @@ namespace pkv {
 // 16-token boxes; the concatenated streams are cut into equal contiguous
 // slices, one per worker (a consumer warp).
 constexpr int kBox = 16;         // tokens per box = per TMA copy; divides every block size
-constexpr int kWorkers = 8;      // consumer warps (workers) per CTA
-constexpr int kDecodeThreads = (kWorkers + 1) * 32;  // + one producer warp
+// Two CTA shapes: four workers (consumer warps) + one producer warp with a
+// 3-stage ring, two CTAs per SM (preferred: less lock-step per stage, two
+// producers per SM); or eight workers + one producer, one CTA per SM, for
+// sizes whose shared memory does not fit twice on an SM.
+constexpr int kPairWorkers = 4;
+constexpr int kPairStages = 3;
+constexpr int kWideWorkers = 8;
 constexpr int kMaxStages = 4;    // pipeline depth cap (stage = one box per worker)
 constexpr int kMinStages = 2;
+constexpr size_t kSmemPerSm = 228 * 1024;   // shared memory per SM
+constexpr size_t kSmemReserve = 1024;       // reserved per resident CTA
+constexpr size_t kMaxDynSmem = 227 * 1024;  // opt-in maximum per CTA
 constexpr int kMaxBatch = 8192;  // sequences per call (their prefix sums live in shared memory)
 constexpr int kWsHeaderInts = 4; // workspace header: T, P, W, B
 

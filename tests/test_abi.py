@@ -47,11 +47,14 @@ def test_host_only_entry_points(cuda_lib_path):
     f.restype = ctypes.c_size_t
     f.argtypes = [ctypes.c_int] * 7
     hdr = lambda B: (4 + B + 1) * 4 + (-(4 + B + 1) * 4) % 256
-    # 4 seqs x 2 KV heads x 19 boxes = 152 boxes -> 19 CTAs of 8 workers, 2 slots of 2 x (64 + 4) floats
-    assert f(4, 4, 2, 64, 19, 16, 0) == hdr(4) + 19 * 8 * 2 * 2 * 68 * 4
-    # large problems: capped at 256 CTAs; max_ctas caps further
-    assert f(64, 16, 8, 128, 16, 256, 0) == hdr(64) + 256 * 8 * 2 * 2 * 132 * 4
-    assert f(64, 16, 8, 128, 16, 256, 10) == hdr(64) + 10 * 8 * 2 * 2 * 132 * 4
+    # 4 seqs x 2 KV heads x 19 boxes = 152 boxes -> 38 CTAs of 4 workers (two CTAs fit an SM);
+    # two partial slots per worker of G x (D + 4) floats
+    assert f(4, 4, 2, 64, 19, 16, 0) == hdr(4) + 38 * 4 * 2 * 2 * 68 * 4
+    # large problems: capped at 2048 workers; max_ctas caps further
+    assert f(64, 16, 8, 128, 16, 256, 0) == hdr(64) + 512 * 4 * 2 * 2 * 132 * 4
+    assert f(64, 16, 8, 128, 16, 256, 10) == hdr(64) + 10 * 4 * 2 * 2 * 132 * 4
+    # G = 8 at D = 128 does not fit two CTAs per SM: 8-worker CTAs
+    assert f(64, 64, 8, 128, 16, 256, 10) == hdr(64) + 10 * 8 * 2 * 8 * 132 * 4
     assert f(-1, 4, 2, 64, 19, 16, 0) == 0
     assert f(0, 4, 2, 64, 19, 16, 0) == 0
     assert f(4, 6, 4, 64, 19, 16, 0) == 0  # Hq not a multiple of Hkv
