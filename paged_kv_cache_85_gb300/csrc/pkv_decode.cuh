@@ -11,8 +11,9 @@
 //  * Work decomposition (stream-K).  Each (sequence, KV head) context is a
 //    stream of 16-token boxes; all G query heads of the group ride along, so
 //    every K/V byte is read from HBM once.  The streams are concatenated
-//    (sequence-major) and the resulting box range is cut into equal
-//    contiguous slices, one per worker; a worker is one consumer warp, and a
+//    (KV-head-major); each head's region is cut into equal contiguous
+//    slices, one per worker, so the workers of different heads read the
+//    same token rows at the same time; a worker is one consumer warp, and a
 //    persistent grid of CTAs with eight workers each fills the 152 SMs.
 //    Every worker therefore moves the same number of bytes (+-1 box), and a
 //    stream is split only where a slice boundary falls into it.  Each CTA
@@ -148,38 +149,42 @@ template <> struct GroupLog2<2> { static constexpr int v = 1; };
 template <> struct GroupLog2<4> { static constexpr int v = 2; };
 template <> struct GroupLog2<8> { static constexpr int v = 3; };
 
-// Box x of the concatenated streams -> (sequence b, KV head h, box j of the
-// stream).  pb[b] = boxes per KV head before sequence b; x < pb[B] * Hkv.
-__device__ __forceinline__ void locate_box(int x, const int *pb, int B, int Hkv, int &b, int &h,
-                                           int &j)
+// Streams are concatenated head-major: all sequences' streams of KV head 0,
+// then of head 1, ...  Workers in different head regions then sit at the
+// same (sequence, box) positions at the same time, so the Hkv slices of one
+// token range are fetched together (DRAM row locality), and sequences that
+// share prefix blocks read them together (L2 reuse).
+// Box x -> (sequence b, KV head h, box j of the stream); pb[b] = boxes per
+// KV head before sequence b, so each head region holds pb[B] boxes.
+__device__ __forceinline__ void locate_box(int x, const int *pb, int B, int &b, int &h, int &j)
 {
-    int lo = 0, hi = B - 1;  // largest b with pb[b] * Hkv <= x (skips empty sequences)
+    const int per_head = pb[B];
+    h = x / per_head;
+    const int r = x - h * per_head;
+    int lo = 0, hi = B - 1;  // largest b with pb[b] <= r (skips empty sequences)
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (pb[mid] * Hkv <= x)
+        if (pb[mid] <= r)
             lo = mid;
         else
             hi = mid - 1;
     }
     b = lo;
-    const int nb = pb[b + 1] - pb[b];
-    const int r = x - pb[b] * Hkv;
-    h = r / nb;
-    j = r - h * nb;
+    j = r - pb[b];
 }
 
 // Advance a (sequence, KV head, box) cursor to the next box of the
 // concatenated streams, skipping sequences without boxes.
-__device__ __forceinline__ void next_box(const int *pb, int B, int Hkv, int &b, int &h, int &j)
+__device__ __forceinline__ void next_box(const int *pb, int B, int &b, int &h, int &j)
 {
     if (++j == pb[b + 1] - pb[b]) {
         j = 0;
-        if (++h == Hkv) {
-            h = 0;
-            ++b;
-            while (b < B && pb[b + 1] == pb[b])
-                ++b;
-        }
+        do {
+            if (++b == B) {
+                b = 0;
+                ++h;
+            }
+        } while (pb[b + 1] == pb[b]);  // ends: the sequence just left has boxes
     }
 }
 
@@ -197,7 +202,8 @@ __device__ __forceinline__ int box_block(const DecodeParams &p, int b, int j)
 template <int D, int G, int NW>
 __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CUtensorMap *tmv,
                                                 const DecodeParams &p, uint8_t *smem,
-                                                const DecodeSmem &L, int lane, int T, int P)
+                                                const DecodeSmem &L, int lane, int R, int Tr,
+                                                int Wr, int P)
 {
     constexpr unsigned FULL = 0xffffffffu;
     constexpr int kBoxBytes = kBox * D * 2;
@@ -211,14 +217,20 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
         prefetch_tensormap(tmk);
         prefetch_tensormap(tmv);
     }
+    // Worker gw owns slice gw % Wr of region gw / Wr (regions past R idle).
     const bool worker = lane < NW;
-    const long long s0 = ((long long)blockIdx.x * NW + lane) * P;
-    const int start = worker ? (int)(s0 < T ? s0 : T) : T;
-    const int end = worker ? (int)(s0 + P < T ? s0 + P : T) : T;
+    const int gw = blockIdx.x * NW + lane;
+    const int r = gw / Wr;
+    int start = 0, end = 0;
+    if (worker && r < R) {
+        const long long lo = (long long)(gw - r * Wr) * P;
+        start = r * Tr + (int)(lo < Tr ? lo : Tr);
+        end = r * Tr + (int)(lo + P < Tr ? lo + P : Tr);
+    }
     int pos = start;
     int cb = 0, ch = 0, cj = 0;  // issue cursor
     if (start < end)
-        locate_box(start, pb, p.B, p.Hkv, cb, ch, cj);
+        locate_box(start, pb, p.B, cb, ch, cj);
     int lb = cb, lh = ch, lj = cj, lpos = start;  // look-ahead cursor
     int qb[kLookahead];                          // block ids of boxes pos .. pos + kLookahead - 1
 #pragma unroll
@@ -226,7 +238,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
         qb[i] = -1;
         if (lpos < end) {
             qb[i] = box_block(p, lb, lj);
-            next_box(pb, p.B, p.Hkv, lb, lh, lj);
+            next_box(pb, p.B, lb, lh, lj);
         }
         ++lpos;
     }
@@ -273,7 +285,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
             m.flags = flags;
             m.blk = blk;
             // advance both cursors
-            next_box(pb, p.B, p.Hkv, cb, ch, cj);
+            next_box(pb, p.B, cb, ch, cj);
             ++pos;
 #pragma unroll
             for (int i = 0; i + 1 < kLookahead; i++)
@@ -281,7 +293,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
             qb[kLookahead - 1] = -1;
             if (lpos < end) {
                 qb[kLookahead - 1] = box_block(p, lb, lj);
-                next_box(pb, p.B, p.Hkv, lb, lh, lj);
+                next_box(pb, p.B, lb, lh, lj);
             }
             ++lpos;
         } else if (worker) {
@@ -610,12 +622,18 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? 2 : 1)
     int *len = reinterpret_cast<int *>(smem + L.len);
     build_prefix(p, pb, len, reinterpret_cast<int *>(smem + L.scan));  // ends with __syncthreads()
 
-    const int T = pb[p.B] * p.Hkv;           // boxes over all streams
-    const int W = (int)gridDim.x * NW; // workers
-    const int P = T > 0 ? (T + W - 1) / W : 1;
+    // Slicing: with at least one worker per KV head, each head's region of
+    // the concatenated streams gets W / Hkv workers and is cut on its own, so
+    // worker w and worker w + W / Hkv read the same (sequence, box) of two
+    // heads at the same time; otherwise one region spans all heads.
+    const int W = (int)gridDim.x * NW;       // workers
+    const int R = W >= p.Hkv ? p.Hkv : 1;    // regions
+    const int Tr = pb[p.B] * (p.Hkv / R);    // boxes per region
+    const int Wr = W / R;                    // workers per region
+    const int P = Tr > 0 ? (Tr + Wr - 1) / Wr : 1;
 
     if (warp == NW) {
-        decode_producer<D, G, NW>(&tmk, &tmv, p, smem, L, lane, T, P);
+        decode_producer<D, G, NW>(&tmk, &tmv, p, smem, L, lane, R, Tr, Wr, P);
     } else {
         if (blockIdx.x == 0) {
             // Publish the box layout for the merge kernel (after the previous
@@ -624,10 +642,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? 2 : 1)
             for (int i = threadIdx.x; i <= p.B; i += NW * 32)
                 p.ws_hdr[kWsHeaderInts + i] = pb[i];
             if (threadIdx.x == 0) {
-                p.ws_hdr[0] = T;
+                p.ws_hdr[0] = Tr;
                 p.ws_hdr[1] = P;
-                p.ws_hdr[2] = W;
+                p.ws_hdr[2] = Wr;
                 p.ws_hdr[3] = p.B;
+                p.ws_hdr[4] = R;
             }
         }
         decode_consumer<D, G, NW>(p, smem, L, warp, lane);

@@ -26,7 +26,7 @@ constexpr size_t kSmemPerSm = 228 * 1024;   // shared memory per SM
 constexpr size_t kSmemReserve = 1024;       // reserved per resident CTA
 constexpr size_t kMaxDynSmem = 227 * 1024;  // opt-in maximum per CTA
 constexpr int kMaxBatch = 8192;  // sequences per call (their prefix sums live in shared memory)
-constexpr int kWsHeaderInts = 4; // workspace header: T, P, W, B
+constexpr int kWsHeaderInts = 8; // workspace header: Tr, P, Wr, B, R (+ padding)
 
 struct DecodeParams {
     const uint16_t *q;            // bf16 [B, Hq, D]

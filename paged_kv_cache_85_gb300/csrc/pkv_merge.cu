@@ -1,10 +1,11 @@
 // Log-sum-exp merge of the pieces of streams that straddle workers.
 //
-// The decode kernel cut the concatenated (sequence, KV head) box streams
-// into equal slices of P boxes, one per worker.  A stream [s, e) that lies in
-// one slice was finished by its worker and written to `out` directly.  A
-// stream spanning workers w0 = s / P .. w1 = (e - 1) / P left one partial
-// per worker, each (acc_i, m_i, l_i) per query head with
+// The decode kernel concatenated the box streams KV-head-major and cut each
+// region (one per KV head, or one for all heads on tiny grids) into equal
+// slices of P boxes, Wr workers per region.  A stream [s, e) of region r
+// that lies in one slice was finished by its worker and written to `out`
+// directly.  A stream spanning workers r*Wr + s/P .. r*Wr + (e-1)/P left one
+// partial per worker, each (acc_i, m_i, l_i) per query head with
 // acc_i = sum over the piece of 2^(s_t - m_i) v_t and l_i = sum of
 // 2^(s_t - m_i) (scores in log2 units).  Worker w0's piece sits in its first
 // slot if the stream starts its slice, else in its second slot (the last
@@ -41,6 +42,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_pieces_kernel(const De
     // The box layout and the partials come from the decode kernel just before.
     grid_dependency_wait();
     const int P = p.ws_hdr[1];
+    const int Wr = p.ws_hdr[2];
+    const int R = p.ws_hdr[4];
     const int *pb = p.ws_hdr + kWsHeaderInts;
     const int nb = pb[b + 1] - pb[b];
     uint16_t *o = p.out + row * D + lane * DPL;
@@ -50,13 +53,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_pieces_kernel(const De
             o[i] = 0;
         return;
     }
-    const int s = pb[b] * p.Hkv + kvh * nb;
+    // Position of the stream inside its region (one region per KV head, or
+    // a single region holding all heads head-major).
+    const int r = R == p.Hkv ? kvh : 0;
+    const int s = (R == p.Hkv ? 0 : kvh * pb[p.B]) + pb[b];
     const int e = s + nb;
-    const int w0 = s / P, w1 = (e - 1) / P;
+    const int w0 = r * Wr + s / P, w1 = r * Wr + (e - 1) / P;
     if (w0 == w1)
         return;  // finished inside one worker
     const int n = w1 - w0 + 1;
-    const int slot0 = (s == w0 * P) ? 0 : 1;
+    const int slot0 = (s % P == 0) ? 0 : 1;
     auto piece = [&](int i) -> const float * {
         const int w = w0 + i;
         const int slot = i == 0 ? slot0 : 0;

@@ -25,8 +25,6 @@ __global__ void __launch_bounds__(kStoreThreads)
     grid_launch_dependents();
     const int64_t i = blockIdx.x;
     const int64_t slot = __ldg(slot_mapping + i);
-    // The cache may still be read by the previous step's kernels.
-    grid_dependency_wait();
     if (slot == -1)
         return;
     if (slot < 0 || slot >= n_slots) {
@@ -38,7 +36,19 @@ __global__ void __launch_bounds__(kStoreThreads)
     const uint4 *vs = v + i * row16;
     uint4 *kd = k_cache + slot * row16;
     uint4 *vd = v_cache + slot * row16;
-    for (int c = threadIdx.x; c < row16; c += kStoreThreads) {
+    // The new rows are inputs no earlier kernel writes: fetch the first chunk
+    // before waiting on the previous kernels, which may still read the cache.
+    uint4 a0 = make_uint4(0, 0, 0, 0), b0 = a0;
+    if ((int)threadIdx.x < row16) {
+        a0 = __ldg(ks + threadIdx.x);
+        b0 = __ldg(vs + threadIdx.x);
+    }
+    grid_dependency_wait();
+    if ((int)threadIdx.x < row16) {
+        kd[threadIdx.x] = a0;
+        vd[threadIdx.x] = b0;
+    }
+    for (int c = threadIdx.x + kStoreThreads; c < row16; c += kStoreThreads) {
         const uint4 a = __ldg(ks + c);
         const uint4 b = __ldg(vs + c);
         kd[c] = a;

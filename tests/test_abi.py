@@ -46,7 +46,7 @@ def test_host_only_entry_points(cuda_lib_path):
     f = lib.pkv_decode_workspace_bytes
     f.restype = ctypes.c_size_t
     f.argtypes = [ctypes.c_int] * 7
-    hdr = lambda B: (4 + B + 1) * 4 + (-(4 + B + 1) * 4) % 256
+    hdr = lambda B: (8 + B + 1) * 4 + (-(8 + B + 1) * 4) % 256
     # 4 seqs x 2 KV heads x 19 boxes = 152 boxes -> 38 CTAs of 4 workers (two CTAs fit an SM);
     # two partial slots per worker of G x (D + 4) floats
     assert f(4, 4, 2, 64, 19, 16, 0) == hdr(4) + 38 * 4 * 2 * 2 * 68 * 4
