@@ -109,18 +109,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 3-D view of a cache [NB*bs tokens, Hkv, D] with a box of 16 tokens x 1 head x D.
+// 4-D view of a cache [NB*bs tokens, Hkv, D] as (64 columns, D/64 halves,
+// Hkv, tokens); a box is 64 columns x 1 half x 1 head x 16 tokens, landing as
+// 16 rows of 128 B with the 128-byte swizzle (conflict-free ldmatrix reads).
 pkv_status make_cache_map(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc)
         return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)tokens};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
-    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)pkv::kBox};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(cache), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    cuuint64_t dims[4] = {64, (cuuint64_t)(D / 64), (cuuint64_t)Hkv, (cuuint64_t)tokens};
+    cuuint64_t strides[3] = {128, (cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+    cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)pkv::kBox};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);

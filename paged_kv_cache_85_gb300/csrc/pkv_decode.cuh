@@ -26,13 +26,11 @@
 //    the [NB*bs, Hkv, D] cache view) arrive by TMA into a ring of
 //    shared-memory stages completed on mbarriers with their byte counts; the
 //    G query rows of a worker's new piece come with it by a bulk copy.
-//  * Consumer warps (workers).  Scores: 8 lanes share a token (16-byte,
-//    conflict-free reads of the K row); each lane dots its slice of d with
-//    all G query rows in packed fp32 FMAs, and a reduce-scatter across the
-//    8 lanes leaves one (token, head) score per lane.  Online softmax in fp32
-//    (log2 domain, running max and sum per head); probabilities go through a
-//    small per-warp buffer; P.V accumulates in packed fp32 FMAs with each
-//    lane owning D/32 output columns of all G heads.  When a worker finishes
+//  * Consumer warps (workers).  Per box, Q.K^T and P.V run on the tensor
+//    cores as warp-level bf16 MMAs with the G query heads as the rows (one
+//    GQA group per MMA), fp32 accumulation, and the online softmax in fp32
+//    registers (log2 domain); P enters P.V as a bf16 hi + lo pair.  K/V boxes
+//    arrive 128-byte swizzled so the ldmatrix reads are conflict-free.  When a worker finishes
 //    a piece of a stream it either writes the normalised bf16 output (the
 //    piece is the whole stream) or a partial (acc, max, sum) into one of its
 //    two workspace slots (first / last piece of its slice); a second kernel
@@ -50,6 +48,7 @@
 namespace pkv {
 
 constexpr int kLookahead = 4;  // boxes per worker whose block ids are loaded ahead of use
+constexpr int kHalfBytes = kBox * 128;  // one 64-column half of a box: 16 rows of 128 B
 
 // Per-worker box descriptor of a stage, written by the producer.
 struct __align__(16) BoxMeta {
@@ -66,7 +65,7 @@ constexpr int kSlot1 = 64;       // a partial of this piece goes to the worker's
 constexpr int kStageStop = 1 << 30;
 
 struct DecodeSmem {
-    size_t kv, q, pbuf, full, empty, meta, pb, len, scan, total;
+    size_t kv, q, full, empty, meta, pb, len, scan, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -75,12 +74,10 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int NW, i
 {
     DecodeSmem L;
     size_t o = 0;
-    L.kv = o;  // per stage: K boxes [NW][16][D], then V boxes [NW][16][D]
+    L.kv = o;  // per stage: K boxes [NW][D/64][16][64], then V boxes alike (128B-swizzled rows)
     o += (size_t)stages * 2 * NW * kBox * D * 2;
     L.q = o;  // per stage and worker: G query rows
     o = align_up(o + (size_t)stages * NW * G * D * 2, 16);
-    L.pbuf = o;  // per worker: probabilities [16 tokens][G] as (p, p) pairs
-    o = align_up(o + (size_t)NW * kBox * G * 8, 16);
     L.full = o;
     o += (size_t)stages * 8;
     L.empty = o;
@@ -93,7 +90,7 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int NW, i
     o = align_up(o + (size_t)B * 4, 16);
     L.scan = o;  // per-warp partial sums of the prefix scan
     o = align_up(o + (size_t)(NW + 2) * 4, 16);
-    L.total = o;
+    L.total = o + 1024;  // slack to align the base to 1024 B (128-byte swizzle atoms)
     return L;
 }
 
@@ -105,49 +102,6 @@ inline int decode_stages_for(int D, int G, int NW, int B, int max_stages, size_t
             return s;
     return 0;
 }
-
-// Sum of G per-lane partial values over the 8 lanes of a token group, left
-// as one (token, head) value per lane: halving exchanges while more than one
-// head remains, plain butterflies after.  The head a lane ends with is
-// (lane & 7) >> (3 - log2 G).
-template <int N> __device__ __forceinline__ void halve(float *x, int lane, int mask)
-{
-    const bool upper = (lane & mask) != 0;
-#pragma unroll
-    for (int i = 0; i < N / 2; i++) {
-        const float send = upper ? x[i] : x[i + N / 2];
-        const float keep = upper ? x[i + N / 2] : x[i];
-        x[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-    }
-}
-
-template <int G> __device__ __forceinline__ float reduce_scatter8(float (&x)[G], int lane)
-{
-    if constexpr (G == 8) {
-        halve<8>(x, lane, 4);
-        halve<4>(x, lane, 2);
-        halve<2>(x, lane, 1);
-    } else if constexpr (G == 4) {
-        halve<4>(x, lane, 4);
-        halve<2>(x, lane, 2);
-        x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
-    } else if constexpr (G == 2) {
-        halve<2>(x, lane, 4);
-        x[0] += __shfl_xor_sync(0xffffffffu, x[0], 2);
-        x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
-    } else {
-        x[0] += __shfl_xor_sync(0xffffffffu, x[0], 4);
-        x[0] += __shfl_xor_sync(0xffffffffu, x[0], 2);
-        x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
-    }
-    return x[0];
-}
-
-template <int G> struct GroupLog2;
-template <> struct GroupLog2<1> { static constexpr int v = 0; };
-template <> struct GroupLog2<2> { static constexpr int v = 1; };
-template <> struct GroupLog2<4> { static constexpr int v = 2; };
-template <> struct GroupLog2<8> { static constexpr int v = 3; };
 
 // Streams are concatenated head-major: all sequences' streams of KV head 0,
 // then of head 1, ...  Workers in different head regions then sit at the
@@ -309,8 +263,12 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
                       p.q + ((size_t)b * p.Hq + (size_t)h * G) * D, G * D * 2, &full[stage]);
         if (flags & kBoxLoaded) {
             uint8_t *kd = smem + L.kv + ((size_t)stage * 2 * NW + lane) * kBoxBytes;
-            tma_load_3d(kd, tmk, 0, h, row, &full[stage]);
-            tma_load_3d(kd + (size_t)NW * kBoxBytes, tmv, 0, h, row, &full[stage]);
+#pragma unroll
+            for (int half = 0; half < D / 64; half++) {
+                tma_load_4d(kd + half * kHalfBytes, tmk, 0, half, h, row, &full[stage]);
+                tma_load_4d(kd + (size_t)NW * kBoxBytes + half * kHalfBytes, tmv, 0, half, h, row,
+                            &full[stage]);
+            }
         }
         if (++stage == p.stages) {
             stage = 0;
@@ -330,43 +288,52 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
         mbar_arrive(&full[stage]);
 }
 
+// Byte offset of 16-byte chunk `c` (0 .. D/8-1) of token row `t` inside a box
+// stored as D/64 halves of [16 rows][128 B] with the 128-byte TMA swizzle
+// (chunk index XOR row % 8 within each row).
+__device__ __forceinline__ uint32_t box_chunk(int t, int c)
+{
+    return (uint32_t)((c >> 3) * kHalfBytes + t * 128 + (((c & 7) ^ (t & 7)) << 4));
+}
+
+// Consumer warp (worker).  Per 16-token box, on the tensor cores
+// (mma.sync m16n8k16, bf16 in, fp32 accumulate), with the G query heads as
+// the M rows (zero-padded to 16):
+//   S[G x 16] = Q[G x D] . K^T    16 MMAs (D=128), K fragments by ldmatrix
+//   online softmax in fp32 on the S fragments (each lane owns one head's row)
+//   O[G x D] += P . V             P split into bf16 hi + lo parts (2 MMAs per
+//                                 n-tile) so P keeps ~16 mantissa bits; V
+//                                 fragments by ldmatrix.trans
 template <int D, int G, int NW>
 __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *smem,
                                                 const DecodeSmem &L, int warp, int lane)
 {
-    constexpr int NCH = D / 64;      // 16-byte K chunks per lane per token (2 or 1)
-    constexpr int EP = NCH * 4;      // packed fp32 pairs of q per head per lane
-    constexpr int DPL = D / 32;      // output columns per lane
-    constexpr int VP = DPL / 2;      // packed pairs of output columns
-    constexpr int HSHIFT = 3 - GroupLog2<G>::v;
+    constexpr int KSTEPS = D / 16;   // k-steps of the score MMA
+    constexpr int NT = D / 8;        // 8-column n-tiles of the output
     constexpr int kBoxBytes = kBox * D * 2;
-    constexpr int kRowBytes = D * 2;
     constexpr unsigned FULL = 0xffffffffu;
 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
     const BoxMeta *meta = reinterpret_cast<const BoxMeta *>(smem + L.meta);
-    float2 *pbuf = reinterpret_cast<float2 *>(smem + L.pbuf) + warp * kBox * G;
 
-    const int r = lane & 7;        // position within the 8-lane token group
-    const int slot = lane >> 3;    // which of 4 tokens this lane scores per step
-    const int hsel = r >> HSHIFT;  // head of this lane's score after the reduction
-    const bool leader = (r & ((1 << HSHIFT) - 1)) == 0;
+    const int hrow = lane >> 2;    // head row of this lane's accumulator fragments
+    const int quad = lane & 3;     // column pair within a fragment
+    const bool real = hrow < G;    // rows G..15 are padding
+    const int mat = lane >> 3;     // ldmatrix: matrix whose row address this lane supplies
+    const int mrow = lane & 7;
     const int gw = blockIdx.x * NW + warp;
 
-    float2 qv[G][EP];
-    float2 acc[G][VP];
+    uint32_t qa[KSTEPS][2];        // A fragments of q (a0, a2); a1 = a3 = 0 (padding rows)
+    float o[NT][4];
     float m_run = -INFINITY, l_run = 0.f;
-    bool whole = false;  // the current piece began at its stream's first box
+    bool whole = false;            // the current piece began at its stream's first box
 #pragma unroll
-    for (int g = 0; g < G; g++) {
+    for (int k = 0; k < KSTEPS; k++)
+        qa[k][0] = qa[k][1] = 0u;
 #pragma unroll
-        for (int i = 0; i < EP; i++)
-            qv[g][i] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < VP; i++)
-            acc[g][i] = make_float2(0.f, 0.f);
-    }
+    for (int n = 0; n < NT; n++)
+        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
     int stage = 0;
     uint32_t phase = 0;
@@ -381,118 +348,89 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *
             break;
         if (bm.flags & kPieceFirst) {
             const uint8_t *qs = smem + L.q + ((size_t)stage * NW + warp) * G * D * 2;
-            const float2 sc = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-            for (int g = 0; g < G; g++)
-#pragma unroll
-                for (int ch = 0; ch < NCH; ch++) {
-                    const uint4 w4 =
-                        *reinterpret_cast<const uint4 *>(qs + (g * D + ch * 64 + r * 8) * 2);
-                    qv[g][ch * 4 + 0] = __fmul2_rn(bf16x2_to_float2(w4.x), sc);
-                    qv[g][ch * 4 + 1] = __fmul2_rn(bf16x2_to_float2(w4.y), sc);
-                    qv[g][ch * 4 + 2] = __fmul2_rn(bf16x2_to_float2(w4.z), sc);
-                    qv[g][ch * 4 + 3] = __fmul2_rn(bf16x2_to_float2(w4.w), sc);
-                }
+            for (int k = 0; k < KSTEPS; k++) {
+                qa[k][0] = real ? *reinterpret_cast<const uint32_t *>(
+                                      qs + (hrow * D + k * 16 + 2 * quad) * 2)
+                                : 0u;
+                qa[k][1] = real ? *reinterpret_cast<const uint32_t *>(
+                                      qs + (hrow * D + k * 16 + 8 + 2 * quad) * 2)
+                                : 0u;
+            }
             m_run = -INFINITY;
             l_run = 0.f;
 #pragma unroll
-            for (int g = 0; g < G; g++)
-#pragma unroll
-                for (int i = 0; i < VP; i++)
-                    acc[g][i] = make_float2(0.f, 0.f);
+            for (int n = 0; n < NT; n++)
+                o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
             whole = (bm.flags & kStreamFirst) != 0;
         }
         const int nvw = (bm.flags & kBoxLoaded) ? bm.nvalid : 0;
         if (nvw > 0) {
-            const uint8_t *Ks = smem + L.kv + ((size_t)stage * 2 * NW + warp) * kBoxBytes;
-            const uint8_t *Vs = Ks + (size_t)NW * kBoxBytes;
-            // ---- scores for the box's 16 tokens (4 per step) ----
-            float sv[4];
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int tt = 4 * j + slot;
-                const uint8_t *row = Ks + tt * kRowBytes;
-                float2 kf[EP];
-#pragma unroll
-                for (int ch = 0; ch < NCH; ch++) {
-                    const uint4 w4 = *reinterpret_cast<const uint4 *>(row + ch * 128 + r * 16);
-                    kf[ch * 4 + 0] = bf16x2_to_float2(w4.x);
-                    kf[ch * 4 + 1] = bf16x2_to_float2(w4.y);
-                    kf[ch * 4 + 2] = bf16x2_to_float2(w4.z);
-                    kf[ch * 4 + 3] = bf16x2_to_float2(w4.w);
+            uint8_t *Ks = smem + L.kv + ((size_t)stage * 2 * NW + warp) * kBoxBytes;
+            uint8_t *Vs = Ks + (size_t)NW * kBoxBytes;
+            if (nvw < kBox) {
+                // Rows past the context take weight 0, and 0 * NaN would still be
+                // NaN on the tensor cores: clear them (whole rows, any swizzle).
+                for (int i = lane; i < (kBox - nvw) * (D / 8); i += 32) {
+                    const int t = nvw + i / (D / 8), c = i % (D / 8);
+                    *reinterpret_cast<uint4 *>(Vs + (c >> 3) * kHalfBytes + t * 128 + (c & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 }
-                float part[G];
-#pragma unroll
-                for (int g = 0; g < G; g++) {
-                    float2 a = __fmul2_rn(qv[g][0], kf[0]);
-#pragma unroll
-                    for (int i = 1; i < EP; i++)
-                        a = __ffma2_rn(qv[g][i], kf[i], a);
-                    part[g] = a.x + a.y;
-                }
-                const float s = reduce_scatter8<G>(part, lane);
-                sv[j] = tt < nvw ? s : -INFINITY;
+                fence_proxy_async_smem();  // before TMA refills this buffer
+                __syncwarp();
             }
-            // ---- online softmax (log2 domain) ----
+            const uint32_t kb = smem_u32(Ks), vb = smem_u32(Vs);
+            // ---- scores S = Q K^T (two 8-token n-tiles) ----
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const int ktok = mrow + ((mat >> 1) << 3);
+#pragma unroll
+            for (int k = 0; k < KSTEPS; k++) {
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(kb + box_chunk(ktok, 2 * k + (mat & 1)), b0, b1, b2, b3);
+                mma_bf16_16816(sc[0], qa[k][0], 0u, qa[k][1], 0u, b0, b1);
+                mma_bf16_16816(sc[1], qa[k][0], 0u, qa[k][1], 0u, b2, b3);
+            }
+            // ---- online softmax (log2 domain); this lane: head hrow, tokens
+            //      2q, 2q+1, 8+2q, 9+2q ----
+            float sv[4] = {sc[0][0], sc[0][1], sc[1][0], sc[1][1]};
+            const int tq = 2 * quad;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int t = tq + (i & 1) + ((i >> 1) << 3);
+                sv[i] = t < nvw ? sv[i] * p.scale_log2 : -INFINITY;
+            }
             float mt = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-            mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 8));
-            mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 16));
+            mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 2));
             const float m_new = fmaxf(m_run, mt);
             const float alpha = fast_exp2(m_run - m_new);
             m_run = m_new;
-            float psum = 0.f;
+            float pr[4];
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const float pj = fast_exp2(sv[j] - m_new);
-                psum += pj;
-                if (leader)
-                    pbuf[(4 * j + slot) * G + hsel] = make_float2(pj, pj);
+            for (int i = 0; i < 4; i++)
+                pr[i] = real ? fast_exp2(sv[i] - m_new) : 0.f;
+            l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+#pragma unroll
+            for (int n = 0; n < NT; n++) {
+                o[n][0] *= alpha;
+                o[n][1] *= alpha;
             }
-            l_run = l_run * alpha + psum;
+            // ---- P as A fragments, split hi + lo ----
+            const uint32_t ph0 = pack_bf16x2(pr[0], pr[1]);
+            const uint32_t ph2 = pack_bf16x2(pr[2], pr[3]);
+            const float2 h0 = bf16x2_to_float2(ph0), h2 = bf16x2_to_float2(ph2);
+            const uint32_t pl0 = pack_bf16x2(pr[0] - h0.x, pr[1] - h0.y);
+            const uint32_t pl2 = pack_bf16x2(pr[2] - h2.x, pr[3] - h2.y);
+            // ---- O += P V ----
+            const int vtok = mrow + ((mat & 1) << 3);
 #pragma unroll
-            for (int g = 0; g < G; g++) {
-                const float ag = __shfl_sync(FULL, alpha, g << HSHIFT);
-                const float2 a2 = make_float2(ag, ag);
-#pragma unroll
-                for (int i = 0; i < VP; i++)
-                    acc[g][i] = __fmul2_rn(acc[g][i], a2);
-            }
-            __syncwarp();
-            // ---- P.V ----
-            auto pv_step = [&](int t) {
-                float2 pp[G];
-                if constexpr (G == 1) {
-                    pp[0] = pbuf[t];
-                } else {
-#pragma unroll
-                    for (int g = 0; g < G; g += 2) {
-                        const float4 x = *reinterpret_cast<const float4 *>(pbuf + t * G + g);
-                        pp[g] = make_float2(x.x, x.y);
-                        pp[g + 1] = make_float2(x.z, x.w);
-                    }
-                }
-                float2 vf[VP];
-                const uint8_t *vrow = Vs + t * kRowBytes + lane * DPL * 2;
-                if constexpr (VP == 2) {
-                    const uint2 w2 = *reinterpret_cast<const uint2 *>(vrow);
-                    vf[0] = bf16x2_to_float2(w2.x);
-                    vf[1] = bf16x2_to_float2(w2.y);
-                } else {
-                    vf[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(vrow));
-                }
-#pragma unroll
-                for (int g = 0; g < G; g++)
-#pragma unroll
-                    for (int i = 0; i < VP; i++)
-                        acc[g][i] = __ffma2_rn(pp[g], vf[i], acc[g][i]);
-            };
-            if (nvw == kBox) {
-#pragma unroll
-                for (int t = 0; t < kBox; t++)
-                    pv_step(t);
-            } else {
-                for (int t = 0; t < nvw; t++)
-                    pv_step(t);
+            for (int n2 = 0; n2 < NT / 2; n2++) {
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(vb + box_chunk(vtok, 2 * n2 + (mat >> 1)), v0, v1, v2, v3);
+                mma_bf16_16816(o[2 * n2], ph0, 0u, ph2, 0u, v0, v1);
+                mma_bf16_16816(o[2 * n2], pl0, 0u, pl2, 0u, v0, v1);
+                mma_bf16_16816(o[2 * n2 + 1], ph0, 0u, ph2, 0u, v2, v3);
+                mma_bf16_16816(o[2 * n2 + 1], pl0, 0u, pl2, 0u, v2, v3);
             }
         }
         __syncwarp();
@@ -501,40 +439,27 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *
 
         if (bm.flags & kPieceLast) {
             // ---- finish this worker's piece of the stream ----
-            float l_tot = l_run + __shfl_xor_sync(FULL, l_run, 8);
-            l_tot += __shfl_xor_sync(FULL, l_tot, 16);
+            float l_tot = l_run + __shfl_xor_sync(FULL, l_run, 1);
+            l_tot += __shfl_xor_sync(FULL, l_tot, 2);
             const bool complete = whole && (bm.flags & kStreamLast);
-            const size_t row0 = (size_t)bm.b * p.Hq + (size_t)bm.h * G;
-            float *part = p.ws_part +
-                          ((size_t)gw * 2 + ((bm.flags & kSlot1) ? 1 : 0)) * G * (D + 4);
-#pragma unroll
-            for (int g = 0; g < G; g++) {
-                const float mg = __shfl_sync(FULL, m_run, g << HSHIFT);
-                const float lg = __shfl_sync(FULL, l_tot, g << HSHIFT);
+            if (real) {
+                const size_t hq = (size_t)bm.b * p.Hq + (size_t)bm.h * G + hrow;
                 if (complete) {
-                    uint32_t pk[VP];
+                    uint16_t *orow = p.out + hq * D + 2 * quad;
 #pragma unroll
-                    for (int i = 0; i < VP; i++) {
-                        const float x0 = lg > 0.f ? acc[g][i].x / lg : 0.f;
-                        const float x1 = lg > 0.f ? acc[g][i].y / lg : 0.f;
-                        pk[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x0)) |
-                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x1)) << 16);
-                    }
-                    uint16_t *o = p.out + (row0 + g) * D + lane * DPL;
-                    if constexpr (VP == 2)
-                        *reinterpret_cast<uint2 *>(o) = make_uint2(pk[0], pk[1]);
-                    else
-                        *reinterpret_cast<uint32_t *>(o) = pk[0];
+                    for (int n = 0; n < NT; n++)
+                        *reinterpret_cast<uint32_t *>(orow + 8 * n) =
+                            pack_bf16x2(l_tot > 0.f ? o[n][0] / l_tot : 0.f,
+                                        l_tot > 0.f ? o[n][1] / l_tot : 0.f);
                 } else {
-                    float *pg = part + (size_t)g * (D + 4);
-                    if constexpr (VP == 2)
-                        *reinterpret_cast<float4 *>(pg + lane * DPL) =
-                            make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
-                    else
-                        *reinterpret_cast<float2 *>(pg + lane * DPL) = acc[g][0];
-                    if (lane == 0) {
-                        pg[D] = mg;
-                        pg[D + 1] = lg;
+                    float *pg = p.ws_part +
+                                (((size_t)gw * 2 + ((bm.flags & kSlot1) ? 1 : 0)) * G + hrow) * (D + 4);
+#pragma unroll
+                    for (int n = 0; n < NT; n++)
+                        *reinterpret_cast<float2 *>(pg + 8 * n + 2 * quad) = make_float2(o[n][0], o[n][1]);
+                    if (quad == 0) {
+                        pg[D] = m_run;
+                        pg[D + 1] = l_tot;
                     }
                 }
             }
@@ -603,7 +528,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? 2 : 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeParams p)
 {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const DecodeSmem L = decode_smem_layout(D, G, NW, p.stages, p.B);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
