@@ -102,20 +102,31 @@ def _require(t, name, dtype, ndim):
 
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != dtype:
-        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if t.dim() != ndim:
-        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be on a CUDA device")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype or t.dim() != ndim or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor with {ndim} dims; "
+                         f"got {t.dtype}, shape {tuple(t.shape)}, device {t.device}, "
+                         f"contiguous={t.is_contiguous()}")
 
 
-def _stream_ptr(device):
+def _raw_stream(device_index: int):
+    """Handle of the current CUDA stream on `device_index` (no Python Stream object)."""
     import torch
 
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    get = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if get is not None:
+        return get(device_index)
+    return torch.cuda.current_stream(device_index).cuda_stream
+
+
+def _on_device(index: int):
+    """Context that makes `index` the current CUDA device only when it is not already."""
+    import contextlib
+
+    import torch
+
+    if torch.cuda.current_device() == index:
+        return contextlib.nullcontext()
+    return torch.cuda.device(index)
 
 
 def store_kvcache(k, v, k_cache, v_cache, slot_mapping, err_flag=None):
@@ -135,12 +146,13 @@ def store_kvcache(k, v, k_cache, v_cache, slot_mapping, err_flag=None):
         raise ValueError("store_kvcache: slot_mapping length != number of rows")
     if err_flag is not None:
         _require(err_flag, "err_flag", torch.int32, 1)
-    lib = load_library()
-    with torch.cuda.device(k.device):
+    lib = _lib or load_library()
+    idx = k.get_device()
+    with _on_device(idx):
         _check(lib.pkv_store_kvcache(
             k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
             slot_mapping.data_ptr(), N, Hkv, D, NB, bs,
-            err_flag.data_ptr() if err_flag is not None else None, _stream_ptr(k.device)))
+            err_flag.data_ptr() if err_flag is not None else None, _raw_stream(idx)))
 
 
 def decode_workspace_bytes(B, Hq, Hkv, D, MBS, bs, max_ctas=0) -> int:
@@ -186,12 +198,13 @@ def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ou
     MBS = block_tables.shape[1]
     if err_flag is not None:
         _require(err_flag, "err_flag", torch.int32, 1)
-    lib = load_library()
-    with torch.cuda.device(q.device):
-        stream = _stream_ptr(q.device)
-        need = int(lib.pkv_decode_workspace_bytes(B, Hq, Hkv, D, max(MBS, 1), bs, max_ctas))
+    lib = _lib or load_library()
+    idx = q.get_device()
+    with _on_device(idx):
+        stream = _raw_stream(idx)
         if workspace is None:
-            workspace = _workspace(q.device, stream.value, need)
+            need = int(lib.pkv_decode_workspace_bytes(B, Hq, Hkv, D, max(MBS, 1), bs, max_ctas))
+            workspace = _workspace(q.device, stream, need)
         ws_ptr = workspace.data_ptr() if workspace is not None else None
         ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
         _check(lib.pkv_paged_attn_decode(

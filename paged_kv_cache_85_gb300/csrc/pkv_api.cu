@@ -68,6 +68,7 @@ using pkv::kMaxDynSmem;
 
 struct DeviceState {
     bool ready = false;
+    int dev = 0;
     int sms = 0;
     bool smem_set[2][2][9] = {};  // [D == 128][NW == 8][G]
 };
@@ -88,6 +89,7 @@ pkv_status device_state(DeviceState **out)
         e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess)
             return fail(PKV_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        st.dev = dev;
         st.ready = true;
     }
     *out = &st;
@@ -109,6 +111,41 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
+// Occupancy per (kernel, dynamic shared memory), cached: the query is pure
+// host arithmetic but not free, and decode calls repeat the same shapes.
+struct OccEntry {
+    const void *fn = nullptr;
+    size_t smem = 0;
+    int occ = 0;
+};
+constexpr int kOccCache = 32;
+OccEntry g_occ[kMaxDevices][kOccCache];
+
+pkv_status occupancy(int dev, const void *fn, int threads, size_t smem, int *occ)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    OccEntry *slot = nullptr;
+    for (auto &e : g_occ[dev]) {
+        if (e.fn == fn && e.smem == smem) {
+            *occ = e.occ;
+            return PKV_OK;
+        }
+        if (!e.fn && !slot)
+            slot = &e;
+    }
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
+    if (e != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+    if (slot) {
+        slot->fn = fn;
+        slot->smem = smem;
+        slot->occ = n;
+    }
+    *occ = n;
+    return PKV_OK;
+}
+
 // 4-D view of a cache [NB*bs tokens, Hkv, D] as (64 columns, D/64 halves,
 // Hkv, tokens); a box is 64 columns x 1 half x 1 head x 16 tokens, landing as
 // 16 rows of 128 B with the 128-byte swizzle (conflict-free ldmatrix reads).
@@ -126,6 +163,38 @@ pkv_status make_cache_map(CUtensorMap *map, const void *cache, long long tokens,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+// Tensor maps of recently used caches, per host thread (a map is plain data:
+// the same cache pointer and shape always encode the same map).
+struct MapEntry {
+    const void *ptr = nullptr;
+    long long tokens = 0;
+    int Hkv = 0, D = 0;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 8;
+thread_local MapEntry t_maps[kMapCache];
+thread_local int t_map_next = 0;
+
+pkv_status cached_cache_map(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D)
+{
+    for (const auto &e : t_maps)
+        if (e.ptr == cache && e.tokens == tokens && e.Hkv == Hkv && e.D == D) {
+            *map = e.map;
+            return PKV_OK;
+        }
+    const pkv_status ps = make_cache_map(map, cache, tokens, Hkv, D);
+    if (ps != PKV_OK)
+        return ps;
+    MapEntry &e = t_maps[t_map_next];
+    t_map_next = (t_map_next + 1) % kMapCache;
+    e.ptr = cache;
+    e.tokens = tokens;
+    e.Hkv = Hkv;
+    e.D = D;
+    e.map = *map;
     return PKV_OK;
 }
 
@@ -209,10 +278,8 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
         }
     }
     int occ = 0;
-    cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kfn, (NW + 1) * 32, plan->smem);
-    if (e != cudaSuccess)
-        return fail(PKV_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+    if ((ps = occupancy(st->dev, kfn, (NW + 1) * 32, plan->smem, &occ)) != PKV_OK)
+        return ps;
     if (occ < 1)
         return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: kernel does not fit on an SM");
     const long long resident = (long long)st->sms * occ;
@@ -322,9 +389,9 @@ pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void 
 
     CUtensorMap tmk, tmv;
     const long long tokens = (long long)NB * bs;
-    if ((ps = make_cache_map(&tmk, k_cache, tokens, Hkv, D)) != PKV_OK)
+    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D)) != PKV_OK)
         return ps;
-    if ((ps = make_cache_map(&tmv, v_cache, tokens, Hkv, D)) != PKV_OK)
+    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D)) != PKV_OK)
         return ps;
 
     pkv::DecodeParams p;

@@ -52,3 +52,18 @@ def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.run_reference(bench.parse_args(["--impl", "reference", "--steps", "1", "--warmup", "0"])) is None
     assert capsys.readouterr().out == ""
+
+
+def test_stage_inputs_round_trip_on_cpu():
+    """One packed buffer carries every input: copying it fills all views."""
+    import torch
+
+    host = {"a": torch.arange(7, dtype=torch.int64), "b": torch.randn(3, 5).to(torch.bfloat16),
+            "c": torch.tensor([1, -1], dtype=torch.int32)}
+    packed, views, dev_buf = bench.stage_inputs(host, torch.device("cpu"), pin=False)
+    assert packed.numel() == 256 * 3  # each slice padded to 256 bytes
+    for v in views.values():
+        assert v.data_ptr() % 256 == 0 or v.data_ptr() % 16 == 0
+    dev_buf.copy_(packed)
+    for k, t in host.items():
+        assert torch.equal(views[k], t)
