@@ -56,6 +56,17 @@ def _load():
             lib.oracle_paged_attn_decode.restype = i64
             lib.oracle_paged_attn_decode.argtypes = [
                 P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32, f32, P]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_e4m3_encode.argtypes = [f32]
+            lib.oracle_e4m3_decode.restype = ctypes.c_double
+            lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_store_kvcache_fp8.restype = i64
+            lib.oracle_store_kvcache_fp8.argtypes = [P, P, P, P, P, i64, i32, i32, i64, i32, f32, f32]
+            lib.oracle_dequant_fp8.restype = None
+            lib.oracle_dequant_fp8.argtypes = [P, i64, f32, P]
+            lib.oracle_paged_attn_decode_pairs_f64kv.restype = i64
+            lib.oracle_paged_attn_decode_pairs_f64kv.argtypes = [
+                P, P, P, P, i32, P, i32, i32, i32, i64, i32, f32, P, i64, P]
             lib.oracle_dense_attn.restype = None
             lib.oracle_dense_attn.argtypes = [P, P, P, i32, i32, i32, i32, f32, P]
             _lib = lib
@@ -153,3 +164,71 @@ def dense_attn(q, k, v, scale):
     out = np.zeros((Hq, D), dtype=np.float64)
     lib.oracle_dense_attn(_ptr(q), _ptr(k), _ptr(v), n, Hq, Hkv, D, float(scale), _ptr(out))
     return out
+
+
+# ---------------------------------------------------------------- FP8 cache
+
+
+def e4m3_encode(x: float) -> int:
+    """OCP E4M3 code of an fp32 value (nearest, ties to even, saturating)."""
+    return int(_load().oracle_e4m3_encode(float(np.float32(x))))
+
+
+def e4m3_decode(code: int) -> float:
+    return float(_load().oracle_e4m3_decode(int(code)))
+
+
+def store_kvcache_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale):
+    """Quantize new bf16 K/V rows into copies of uint8 (E4M3) caches."""
+    lib = _load()
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    kc = np.array(k_cache, dtype=np.uint8, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint8, copy=True, order="C")
+    slots = _c(slot_mapping, np.int64)
+    NB, bs, Hkv, D = kc.shape
+    N = slots.shape[0]
+    bad = lib.oracle_store_kvcache_fp8(_ptr(k), _ptr(v), _ptr(kc), _ptr(vc), _ptr(slots), N, Hkv,
+                                       D, NB, bs, float(k_scale), float(v_scale))
+    return kc, vc, int(bad)
+
+
+def dequant_fp8(codes, scale):
+    """fp64 values of E4M3 codes times scale."""
+    lib = _load()
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib.oracle_dequant_fp8(_ptr(c), c.size, float(scale), _ptr(out))
+    return out
+
+
+def paged_attn_decode_values(q, k_vals, v_vals, block_tables, context_lens, scale, pairs=None):
+    """fp64 decode attention over caches holding fp64 values [NB, bs, Hkv, D]."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    kv = _c(k_vals, np.float64)
+    vv = _c(v_vals, np.float64)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = kv.shape
+    assert D2 == D and vv.shape == kv.shape and Hq % Hkv == 0
+    if pairs is None:
+        pr = np.array([(b, h) for b in range(B) for h in range(Hq)], np.int32)
+    else:
+        pr = _c(pairs, np.int32).reshape(-1, 2)
+    out = np.zeros((pr.shape[0], D), dtype=np.float64)
+    bad = lib.oracle_paged_attn_decode_pairs_f64kv(
+        _ptr(q), _ptr(kv), _ptr(vv), _ptr(bt), bt.shape[1], _ptr(cl), Hq, Hkv, D, NB, bs,
+        float(scale), _ptr(pr), pr.shape[0], _ptr(out))
+    if bad < 0:
+        raise MemoryError("oracle allocation failed")
+    return out.reshape(B, Hq, D) if pairs is None else out
+
+
+def paged_attn_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale,
+                          v_scale, pairs=None):
+    """fp64 decode attention over FP8 caches (dequantized K and V)."""
+    kd = dequant_fp8(k_cache, k_scale)
+    vd = dequant_fp8(v_cache, v_scale)
+    return paged_attn_decode_values(q, kd, vd, block_tables, context_lens, scale, pairs=pairs)

@@ -236,3 +236,156 @@ void oracle_dense_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     }
     free(s);
 }
+
+/*
+ * FP8 KV cache ("VLLM-0.7.3 源码" section 5.3: the KV cache may be stored in
+ * FP8 via kv_cache_dtype while the attention computes in higher precision).
+ * The page gives no scale convention; this oracle takes the plain per-tensor
+ * one: a cache value is the OCP E4M3 code of x * (1 / scale) (computed in
+ * fp32), and its value is code_value * scale.
+ *
+ * E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits;
+ * exponent field 0 encodes subnormals m/8 * 2^-6; no infinities; the codes
+ * S.1111.111 are NaN, so the largest finite magnitude is 1.75 * 2^8 = 448.
+ * Quantization rounds to nearest, ties to even, and saturates finite
+ * overflow (and infinities) to +-448; NaN maps to 0x7F with its sign.
+ */
+static double e4m3_value(uint8_t code)
+{
+    int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(float x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    if (isnan(x))
+        return sign | 0x7F;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    /* nearest of all finite magnitudes; ties to the even (mantissa LSB 0) code */
+    uint8_t best = 0;
+    double best_err = a;  /* code 0 has value 0 */
+    for (int c = 1; c <= 0x7E; c++) {
+        double err = fabs(e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = (uint8_t)c;
+            best_err = err;
+        }
+    }
+    return sign | best;
+}
+
+double oracle_e4m3_decode(uint8_t code) { return e4m3_value(code); }
+
+/*
+ * store_kvcache into FP8 caches: every element of k[i] / v[i] (bf16 bits) is
+ * widened, multiplied by 1/k_scale (resp. 1/v_scale) in fp32, and encoded as
+ * E4M3 at the slot slot_mapping[i].  Returns the number of skipped
+ * out-of-range slots.
+ */
+int64_t oracle_store_kvcache_fp8(const uint16_t *k, const uint16_t *v, uint8_t *k_cache,
+                                 uint8_t *v_cache, const int64_t *slot_mapping, int64_t N,
+                                 int Hkv, int D, int64_t NB, int bs, float k_scale, float v_scale)
+{
+    int64_t bad = 0, row = (int64_t)Hkv * D;
+    float kinv = 1.0f / k_scale, vinv = 1.0f / v_scale;
+    for (int64_t i = 0; i < N; i++) {
+        int64_t slot = slot_mapping[i];
+        if (slot == -1)
+            continue;
+        if (slot < 0 || slot >= NB * (int64_t)bs) {
+            bad++;
+            continue;
+        }
+        for (int64_t e = 0; e < row; e++) {
+            float kx = (float)bf16_to_f64(k[i * row + e]) * kinv;
+            float vx = (float)bf16_to_f64(v[i * row + e]) * vinv;
+            k_cache[slot * row + e] = oracle_e4m3_encode(kx);
+            v_cache[slot * row + e] = oracle_e4m3_encode(vx);
+        }
+    }
+    return bad;
+}
+
+/* Dequantize FP8 caches to fp64 (code value * scale). */
+void oracle_dequant_fp8(const uint8_t *codes, int64_t n, float scale, double *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = e4m3_value(codes[i]) * (double)scale;
+}
+
+/*
+ * Decode attention over caches already holding fp64 values (for example
+ * dequantized FP8 codes): the same definition as decode_one, reading K and V
+ * as doubles.  out is [n_pairs, D]; returns the number of pairs that hit an
+ * invalid block-table entry.
+ */
+int64_t oracle_paged_attn_decode_pairs_f64kv(const uint16_t *q, const double *k_cache,
+                                             const double *v_cache, const int32_t *block_tables,
+                                             int MBS, const int32_t *context_lens, int Hq,
+                                             int Hkv, int D, int64_t NB, int bs, float scale,
+                                             const int32_t *pairs, int64_t n_pairs, double *out)
+{
+    int G = Hq / Hkv;
+    int64_t bad = 0;
+    int max_n = MBS * bs;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_n > 0 ? max_n : 1));
+    if (!s)
+        return -1;
+    for (int64_t i = 0; i < n_pairs; i++) {
+        int b = pairs[2 * i], h = pairs[2 * i + 1], kvh = h / G;
+        int n = context_lens[b] > max_n ? max_n : context_lens[b];
+        const uint16_t *qh = q + ((int64_t)b * Hq + h) * D;
+        const int32_t *table = block_tables + (int64_t)b * MBS;
+        double *o = out + i * D;
+        for (int d = 0; d < D; d++)
+            o[d] = 0.0;
+        int ok = 1;
+        for (int t = 0; t < n && ok; t++) {
+            int64_t phys = table[t / bs];
+            if (phys < 0 || phys >= NB) {
+                ok = 0;
+                break;
+            }
+            int64_t base = ((phys * bs + t % bs) * Hkv + kvh) * (int64_t)D;
+            double dot = 0.0;
+            for (int d = 0; d < D; d++)
+                dot += bf16_to_f64(qh[d]) * k_cache[base + d];
+            s[t] = (double)scale * dot;
+        }
+        if (!ok) {
+            bad++;
+            continue;
+        }
+        if (n <= 0)
+            continue;
+        double m = s[0];
+        for (int t = 1; t < n; t++)
+            if (s[t] > m)
+                m = s[t];
+        double l = 0.0;
+        for (int t = 0; t < n; t++) {
+            s[t] = exp(s[t] - m);
+            l += s[t];
+        }
+        for (int t = 0; t < n; t++) {
+            int64_t phys = table[t / bs];
+            int64_t base = ((phys * bs + t % bs) * Hkv + kvh) * (int64_t)D;
+            for (int d = 0; d < D; d++)
+                o[d] += s[t] * v_cache[base + d];
+        }
+        for (int d = 0; d < D; d++)
+            o[d] /= l;
+    }
+    free(s);
+    return bad;
+}
