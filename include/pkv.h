@@ -155,6 +155,48 @@ pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void 
                                  void *stream);
 
 /*
+ * FP8 KV cache ("VLLM-0.7.3 源码" section 5.3: kv_cache_dtype can store the
+ * KV cache in FP8 while the output side keeps higher-precision compute).
+ * The page gives no scale convention; these calls take the plain one: a
+ * cache element is the OCP E4M3 code (1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, no infinities, max 448) of x * (1 / scale), with one
+ * positive fp32 dequant scale per tensor (k_scale for K, v_scale for V), and
+ * stands for code_value * scale.  Caches are uint8 [NB, bs, Hkv, D].
+ */
+
+/*
+ * pkv_store_kvcache_fp8 - quantize and scatter the step's new K/V rows.
+ *
+ * As pkv_store_kvcache, except that each bf16 value x is multiplied by the
+ * fp32 reciprocal of its tensor's scale (1/k_scale, 1/v_scale, each formed
+ * once in IEEE fp32) and stored as the nearest E4M3 code (ties to even;
+ * finite values beyond 448, and infinities, saturate to +-448; NaN stays
+ * NaN).  Hkv*D must be a multiple of 16; scales finite and > 0.
+ */
+pkv_status pkv_store_kvcache_fp8(const void *k, const void *v, void *k_cache, void *v_cache,
+                                 const int64_t *slot_mapping, int64_t N, int Hkv, int D,
+                                 int64_t NB, int bs, float k_scale, float v_scale,
+                                 int32_t *err_flag, void *stream);
+
+/*
+ * pkv_paged_attn_decode_fp8 - pkv_paged_attn_decode over FP8 caches.
+ *
+ * Same arguments, workspace (pkv_decode_workspace_bytes with the same
+ * sizes) and results, reading K = code_value * k_scale and V = code_value *
+ * v_scale.  The contractions run on the tensor cores in f16 with fp32
+ * accumulation (E4M3 values are exact in f16; q is rounded to f16, which is
+ * exact for |q| in [2^-14, 65504] with at most 11 significant bits, i.e. any
+ * bf16 in that range), P in f16, output rounded to bf16.
+ */
+pkv_status pkv_paged_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables, int MBS,
+                                     const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                                     int64_t NB, int bs, float scale, float k_scale,
+                                     float v_scale, void *out, void *workspace,
+                                     size_t workspace_bytes, int max_ctas, int32_t *err_flag,
+                                     void *stream);
+
+/*
  * pkv_paged_attn_decode_noalloc - pkv_paged_attn_decode without a workspace
  * argument, for callers that cannot allocate device memory.
  *

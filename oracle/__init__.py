@@ -193,6 +193,25 @@ def store_kvcache_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale):
     return kc, vc, int(bad)
 
 
+def e4m3_table(scale):
+    """Code of every bf16 bit pattern x for x * (1/scale), as store_kvcache_fp8 writes it.
+
+    The code depends only on x once the scale is fixed, so this is the plain
+    quantizer memoised over all 65536 inputs (one row through the oracle's
+    own store); ``table[bits]`` then quantizes whole caches quickly.
+    """
+    x = np.arange(65536, dtype=np.uint16).reshape(1, 1, 65536)
+    cache = np.zeros((1, 1, 1, 65536), np.uint8)
+    kc, _, bad = store_kvcache_fp8(x, x, cache, cache, np.zeros(1, np.int64), scale, scale)
+    assert bad == 0
+    return kc.reshape(65536)
+
+
+def quantize_bf16(bits, scale):
+    """E4M3 codes of bf16 values (uint16 bits) for a per-tensor scale."""
+    return e4m3_table(scale)[np.asarray(bits, dtype=np.uint16)]
+
+
 def dequant_fp8(codes, scale):
     """fp64 values of E4M3 codes times scale."""
     lib = _load()

@@ -27,6 +27,8 @@ from . import _build
 __all__ = [
     "store_kvcache",
     "paged_attn_decode",
+    "store_kvcache_fp8",
+    "paged_attn_decode_fp8",
     "decode_workspace_bytes",
     "load_library",
     "library_path",
@@ -83,6 +85,11 @@ def load_library():
         lib.pkv_paged_attn_decode.restype = i32
         lib.pkv_paged_attn_decode.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32,
                                               f32, P, P, sz, i32, P, P]
+        lib.pkv_store_kvcache_fp8.restype = i32
+        lib.pkv_store_kvcache_fp8.argtypes = [P, P, P, P, P, i64, i32, i32, i64, i32, f32, f32, P, P]
+        lib.pkv_paged_attn_decode_fp8.restype = i32
+        lib.pkv_paged_attn_decode_fp8.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32,
+                                                  f32, f32, f32, P, P, sz, i32, P, P]
         lib.pkv_last_error.restype = ctypes.c_char_p
         lib.pkv_last_error.argtypes = []
         lib.pkv_version.restype = i32
@@ -211,5 +218,76 @@ def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ou
             q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
             max(MBS, 1), context_lens.data_ptr(), B, Hq, Hkv, D, NB, bs, float(scale),
             out.data_ptr(), ws_ptr, ws_bytes, int(max_ctas),
+            err_flag.data_ptr() if err_flag is not None else None, stream))
+    return out
+
+
+# ---------------------------------------------------------------- FP8 cache
+
+
+def _require_fp8_cache(t, name):
+    import torch
+
+    ok = t.dtype == torch.uint8 or t.dtype == getattr(torch, "float8_e4m3fn", None)
+    if not isinstance(t, torch.Tensor) or not ok or t.dim() != 4 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA uint8 (or float8_e4m3fn) tensor "
+                         f"[NB, bs, Hkv, D]")
+
+
+def store_kvcache_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale, err_flag=None):
+    """Quantize new bf16 K/V rows to E4M3 (per-tensor scales) into FP8 caches."""
+    import torch
+
+    _require(k, "k", torch.bfloat16, 3)
+    _require(v, "v", torch.bfloat16, 3)
+    _require_fp8_cache(k_cache, "k_cache")
+    _require_fp8_cache(v_cache, "v_cache")
+    _require(slot_mapping, "slot_mapping", torch.int64, 1)
+    N, Hkv, D = k.shape
+    NB, bs, Hkv2, D2 = k_cache.shape
+    if v.shape != k.shape or v_cache.shape != k_cache.shape or (Hkv2, D2) != (Hkv, D):
+        raise ValueError("store_kvcache_fp8: shape mismatch between k/v and the caches")
+    if slot_mapping.shape[0] != N:
+        raise ValueError("store_kvcache_fp8: slot_mapping length != number of rows")
+    lib = _lib or load_library()
+    idx = k.get_device()
+    with _on_device(idx):
+        _check(lib.pkv_store_kvcache_fp8(
+            k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+            slot_mapping.data_ptr(), N, Hkv, D, NB, bs, float(k_scale), float(v_scale),
+            err_flag.data_ptr() if err_flag is not None else None, _raw_stream(idx)))
+
+
+def paged_attn_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale,
+                          v_scale, out, max_ctas=0, workspace=None, err_flag=None):
+    """Decode attention over FP8 (E4M3) caches; writes ``out`` and returns it."""
+    import torch
+
+    _require(q, "q", torch.bfloat16, 3)
+    _require_fp8_cache(k_cache, "k_cache")
+    _require_fp8_cache(v_cache, "v_cache")
+    _require(block_tables, "block_tables", torch.int32, 2)
+    _require(context_lens, "context_lens", torch.int32, 1)
+    _require(out, "out", torch.bfloat16, 3)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape:
+        raise ValueError("paged_attn_decode_fp8: shapes do not match")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("paged_attn_decode_fp8: block_tables/context_lens batch != q batch")
+    MBS = block_tables.shape[1]
+    lib = _lib or load_library()
+    idx = q.get_device()
+    with _on_device(idx):
+        stream = _raw_stream(idx)
+        if workspace is None:
+            need = int(lib.pkv_decode_workspace_bytes(B, Hq, Hkv, D, max(MBS, 1), bs, max_ctas))
+            workspace = _workspace(q.device, stream, need)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _check(lib.pkv_paged_attn_decode_fp8(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+            max(MBS, 1), context_lens.data_ptr(), B, Hq, Hkv, D, NB, bs, float(scale),
+            float(k_scale), float(v_scale), out.data_ptr(), ws_ptr, ws_bytes, int(max_ctas),
             err_flag.data_ptr() if err_flag is not None else None, stream))
     return out

@@ -26,22 +26,47 @@ PKV_DECLARE_SHAPE(64, 8)
 PKV_DECLARE_SHAPE(128, 4)
 PKV_DECLARE_SHAPE(128, 8)
 #undef PKV_DECLARE_SHAPE
+#define PKV_DECLARE_SHAPE8(D, NW)                                                                 \
+    cudaError_t launch_decode8_d##D##_w##NW(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,\
+                                            const DecodeParams &p, int grid, size_t smem,         \
+                                            cudaStream_t stream);                                 \
+    const void *decode_kernel8_d##D##_w##NW(int G);
+PKV_DECLARE_SHAPE8(64, 4)
+PKV_DECLARE_SHAPE8(64, 8)
+PKV_DECLARE_SHAPE8(128, 4)
+PKV_DECLARE_SHAPE8(128, 8)
+#undef PKV_DECLARE_SHAPE8
 
-const void *decode_kernel(int D, int NW, int G)
+const void *decode_kernel(int D, int NW, int G, bool f8)
 {
+    const bool pair = NW == kPairWorkers;
+    if (f8) {
+        if (D == 128)
+            return pair ? decode_kernel8_d128_w4(G) : decode_kernel8_d128_w8(G);
+        return pair ? decode_kernel8_d64_w4(G) : decode_kernel8_d64_w8(G);
+    }
     if (D == 128)
-        return NW == kPairWorkers ? decode_kernel_d128_w4(G) : decode_kernel_d128_w8(G);
-    return NW == kPairWorkers ? decode_kernel_d64_w4(G) : decode_kernel_d64_w8(G);
+        return pair ? decode_kernel_d128_w4(G) : decode_kernel_d128_w8(G);
+    return pair ? decode_kernel_d64_w4(G) : decode_kernel_d64_w8(G);
 }
 
-cudaError_t launch_decode(int D, int NW, int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                          const DecodeParams &p, int grid, size_t smem, cudaStream_t stream)
+cudaError_t launch_decode(int D, int NW, int G, bool f8, const CUtensorMap *tmk,
+                          const CUtensorMap *tmv, const DecodeParams &p, int grid, size_t smem,
+                          cudaStream_t stream)
 {
+    const bool pair = NW == kPairWorkers;
+    if (f8) {
+        if (D == 128)
+            return pair ? launch_decode8_d128_w4(G, tmk, tmv, p, grid, smem, stream)
+                        : launch_decode8_d128_w8(G, tmk, tmv, p, grid, smem, stream);
+        return pair ? launch_decode8_d64_w4(G, tmk, tmv, p, grid, smem, stream)
+                    : launch_decode8_d64_w8(G, tmk, tmv, p, grid, smem, stream);
+    }
     if (D == 128)
-        return NW == kPairWorkers ? launch_decode_d128_w4(G, tmk, tmv, p, grid, smem, stream)
-                                  : launch_decode_d128_w8(G, tmk, tmv, p, grid, smem, stream);
-    return NW == kPairWorkers ? launch_decode_d64_w4(G, tmk, tmv, p, grid, smem, stream)
-                              : launch_decode_d64_w8(G, tmk, tmv, p, grid, smem, stream);
+        return pair ? launch_decode_d128_w4(G, tmk, tmv, p, grid, smem, stream)
+                    : launch_decode_d128_w8(G, tmk, tmv, p, grid, smem, stream);
+    return pair ? launch_decode_d64_w4(G, tmk, tmv, p, grid, smem, stream)
+                : launch_decode_d64_w8(G, tmk, tmv, p, grid, smem, stream);
 }
 } // namespace pkv
 
@@ -70,7 +95,7 @@ struct DeviceState {
     bool ready = false;
     int dev = 0;
     int sms = 0;
-    bool smem_set[2][2][9] = {};  // [D == 128][NW == 8][G]
+    bool smem_set[2][2][2][9] = {};  // [fp8][D == 128][NW == 8][G]
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -166,26 +191,50 @@ pkv_status make_cache_map(CUtensorMap *map, const void *cache, long long tokens,
     return PKV_OK;
 }
 
+// FP8 cache [NB*bs tokens, Hkv, D] as bytes: 3-D (D, Hkv, tokens), box
+// D x 1 x 16, swizzled at the row width (128-byte rows for D = 128, 64-byte
+// rows for D = 64).
+pkv_status make_cache_map8(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc)
+        return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)Hkv * D};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)pkv::kBox};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(cache), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (fp8) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
 // Tensor maps of recently used caches, per host thread (a map is plain data:
 // the same cache pointer and shape always encode the same map).
 struct MapEntry {
     const void *ptr = nullptr;
     long long tokens = 0;
     int Hkv = 0, D = 0;
+    bool f8 = false;
     CUtensorMap map;
 };
 constexpr int kMapCache = 8;
 thread_local MapEntry t_maps[kMapCache];
 thread_local int t_map_next = 0;
 
-pkv_status cached_cache_map(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D)
+pkv_status cached_cache_map(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D,
+                            bool f8 = false)
 {
     for (const auto &e : t_maps)
-        if (e.ptr == cache && e.tokens == tokens && e.Hkv == Hkv && e.D == D) {
+        if (e.ptr == cache && e.tokens == tokens && e.Hkv == Hkv && e.D == D && e.f8 == f8) {
             *map = e.map;
             return PKV_OK;
         }
-    const pkv_status ps = make_cache_map(map, cache, tokens, Hkv, D);
+    const pkv_status ps = f8 ? make_cache_map8(map, cache, tokens, Hkv, D)
+                             : make_cache_map(map, cache, tokens, Hkv, D);
     if (ps != PKV_OK)
         return ps;
     MapEntry &e = t_maps[t_map_next];
@@ -194,6 +243,7 @@ pkv_status cached_cache_map(CUtensorMap *map, const void *cache, long long token
     e.tokens = tokens;
     e.Hkv = Hkv;
     e.D = D;
+    e.f8 = f8;
     e.map = *map;
     return PKV_OK;
 }
@@ -208,7 +258,7 @@ struct DecodePlan {
 };
 
 pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_ctas,
-                       bool with_device, DecodePlan *plan)
+                       bool with_device, DecodePlan *plan, bool f8 = false)
 {
     if (B < 1 || Hq < 1 || Hkv < 1 || MBS < 1 || bs < 1 || max_ctas < 0)
         return fail(PKV_ERR_INVALID_ARG,
@@ -233,11 +283,12 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
     // Prefer two 4-worker CTAs per SM; fall back to one 8-worker CTA per SM
     // when two do not fit (large B, or G = 8 with D = 128).
     const size_t pair_smem = pkv::kSmemPerSm / 2 - pkv::kSmemReserve;
+    const int eb = f8 ? 1 : 2;  // bytes per cached element
     int NW = pkv::kPairWorkers;
-    int stages = pkv::decode_stages_for(D, G, NW, B, pkv::kPairStages, pair_smem);
+    int stages = pkv::decode_stages_for(D, G, NW, B, pkv::kPairStages, pair_smem, eb);
     if (stages < pkv::kPairStages) {
         NW = pkv::kWideWorkers;
-        stages = pkv::decode_stages_for(D, G, NW, B, pkv::kMaxStages, kMaxDynSmem);
+        stages = pkv::decode_stages_for(D, G, NW, B, pkv::kMaxStages, kMaxDynSmem, eb);
     }
     if (stages == 0)
         return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: B=%d does not fit shared memory", B);
@@ -251,13 +302,20 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
         grid_cap = max_ctas;
     if (grid_cap < 1)
         grid_cap = 1;
+    // Partial slots: bounded for either CTA shape (and either cache type) by
+    // boxes + 7, by kMaxWorkersTotal, and by max_ctas CTAs of 8 workers.
+    long long workers_cap = box_max + pkv::kWideWorkers - 1;
+    if (workers_cap > kMaxWorkersTotal)
+        workers_cap = kMaxWorkersTotal;
+    if (max_ctas > 0 && workers_cap > (long long)max_ctas * pkv::kWideWorkers)
+        workers_cap = (long long)max_ctas * pkv::kWideWorkers;
     plan->G = G;
     plan->NW = NW;
     plan->stages = stages;
-    plan->smem = pkv::decode_smem_layout(D, G, NW, stages, B).total;
+    plan->smem = pkv::decode_smem_layout(D, G, NW, stages, B, eb).total;
     plan->hdr_bytes = pkv::align_up((size_t)(pkv::kWsHeaderInts + B + 1) * 4, 256);
     plan->ws_bytes = plan->hdr_bytes +
-                     (size_t)grid_cap * NW * 2 * G * (size_t)(D + 4) * sizeof(float);
+                     (size_t)workers_cap * 2 * G * (size_t)(D + 4) * sizeof(float);
     plan->grid = (int)grid_cap;
     if (!with_device)
         return PKV_OK;
@@ -265,10 +323,10 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
     pkv_status ps = device_state(&st);
     if (ps != PKV_OK)
         return ps;
-    const void *kfn = pkv::decode_kernel(D, NW, G);
+    const void *kfn = pkv::decode_kernel(D, NW, G, f8);
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        bool &set = st->smem_set[D == 128][NW == pkv::kWideWorkers][G];
+        bool &set = st->smem_set[f8][D == 128][NW == pkv::kWideWorkers][G];
         if (!set) {
             cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)kMaxDynSmem);
@@ -298,6 +356,78 @@ pkv_status report_error(pkv_status s, const char *msg)
     return fail(s, "%s", msg);
 }
 } // namespace pkv
+
+static pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int MBS, const int32_t *context_lens,
+                              int B, int Hq, int Hkv, int D, int64_t NB, int bs, float scale,
+                              void *out, void *workspace, size_t workspace_bytes, int max_ctas,
+                              int32_t *err_flag, void *stream, bool f8, float k_scale,
+                              float v_scale)
+{
+    if (B < 0 || NB < 1)
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: bad sizes B=%d NB=%lld", B, (long long)NB);
+    if (!std::isfinite(scale))
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: scale is not finite");
+    if (B == 0) {
+        // validate the remaining sizes even though there is nothing to do
+        if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+            return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: bad head counts");
+        return PKV_OK;
+    }
+    if ((long long)NB * bs >= 0x7fffffffLL)
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: NB*bs must be < 2^31");
+    DecodePlan plan;
+    if (f8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale <= 0.f ||
+               v_scale <= 0.f))
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode_fp8: scales must be finite and > 0");
+    pkv_status ps = plan_decode(B, Hq, Hkv, D, MBS, bs, max_ctas, true, &plan, f8);
+    if (ps != PKV_OK)
+        return ps;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: null pointer");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: misaligned pointer");
+    if (!workspace || workspace_bytes < plan.ws_bytes)
+        return fail(PKV_ERR_WORKSPACE, "paged_attn_decode: workspace needs %zu bytes, got %zu",
+                    plan.ws_bytes, workspace ? workspace_bytes : (size_t)0);
+
+    CUtensorMap tmk, tmv;
+    const long long tokens = (long long)NB * bs;
+    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D, f8)) != PKV_OK)
+        return ps;
+    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D, f8)) != PKV_OK)
+        return ps;
+
+    pkv::DecodeParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = static_cast<uint16_t *>(out);
+    p.ws_hdr = static_cast<int32_t *>(workspace);
+    p.ws_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan.hdr_bytes);
+    p.err_flag = err_flag;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.MBS = MBS;
+    p.bs = bs;
+    p.NB = (int)NB;
+    p.stages = plan.stages;
+    p.scale_log2 = scale * 1.4426950408889634f * (f8 ? k_scale : 1.f);
+    p.v_scale = f8 ? v_scale : 1.f;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = pkv::launch_decode(D, plan.NW, plan.G, f8, &tmk, &tmv, p, plan.grid, plan.smem, s);
+    if (e != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "paged_attn_decode launch: %s", cudaGetErrorString(e));
+    e = pkv::launch_merge(D, plan.G, p, s);
+    if (e != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
+
 
 extern "C" {
 
@@ -361,63 +491,55 @@ pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void 
                                  size_t workspace_bytes, int max_ctas, int32_t *err_flag,
                                  void *stream)
 {
-    if (B < 0 || NB < 1)
-        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: bad sizes B=%d NB=%lld", B, (long long)NB);
-    if (!std::isfinite(scale))
-        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: scale is not finite");
-    if (B == 0) {
-        // validate the remaining sizes even though there is nothing to do
-        if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
-            return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: bad head counts");
+    return decode_impl(q, k_cache, v_cache, block_tables, MBS, context_lens, B, Hq, Hkv, D, NB, bs,
+                       scale, out, workspace, workspace_bytes, max_ctas, err_flag, stream, false,
+                       1.f, 1.f);
+}
+
+pkv_status pkv_paged_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables, int MBS,
+                                     const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                                     int64_t NB, int bs, float scale, float k_scale,
+                                     float v_scale, void *out, void *workspace,
+                                     size_t workspace_bytes, int max_ctas, int32_t *err_flag,
+                                     void *stream)
+{
+    return decode_impl(q, k_cache, v_cache, block_tables, MBS, context_lens, B, Hq, Hkv, D, NB, bs,
+                       scale, out, workspace, workspace_bytes, max_ctas, err_flag, stream, true,
+                       k_scale, v_scale);
+}
+
+pkv_status pkv_store_kvcache_fp8(const void *k, const void *v, void *k_cache, void *v_cache,
+                                 const int64_t *slot_mapping, int64_t N, int Hkv, int D,
+                                 int64_t NB, int bs, float k_scale, float v_scale,
+                                 int32_t *err_flag, void *stream)
+{
+    if (N < 0 || Hkv < 1 || D < 1 || NB < 1 || bs < 1)
+        return fail(PKV_ERR_INVALID_ARG, "store_kvcache_fp8: bad sizes");
+    if (N > 0x7fffffffLL)
+        return fail(PKV_ERR_INVALID_ARG, "store_kvcache_fp8: N exceeds 2^31-1");
+    if (((long long)Hkv * D) % 16 != 0)
+        return fail(PKV_ERR_UNSUPPORTED, "store_kvcache_fp8: Hkv*D must be a multiple of 16");
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale <= 0.f || v_scale <= 0.f)
+        return fail(PKV_ERR_INVALID_ARG, "store_kvcache_fp8: scales must be finite and > 0");
+    if (N == 0)
         return PKV_OK;
-    }
-    if ((long long)NB * bs >= 0x7fffffffLL)
-        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: NB*bs must be < 2^31");
-    DecodePlan plan;
-    pkv_status ps = plan_decode(B, Hq, Hkv, D, MBS, bs, max_ctas, true, &plan);
-    if (ps != PKV_OK)
-        return ps;
-    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: null pointer");
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
-        (reinterpret_cast<uintptr_t>(context_lens) & 3u))
-        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode: misaligned pointer");
-    if (!workspace || workspace_bytes < plan.ws_bytes)
-        return fail(PKV_ERR_WORKSPACE, "paged_attn_decode: workspace needs %zu bytes, got %zu",
-                    plan.ws_bytes, workspace ? workspace_bytes : (size_t)0);
-
-    CUtensorMap tmk, tmv;
-    const long long tokens = (long long)NB * bs;
-    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D)) != PKV_OK)
-        return ps;
-    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D)) != PKV_OK)
-        return ps;
-
-    pkv::DecodeParams p;
-    p.q = static_cast<const uint16_t *>(q);
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    p.out = static_cast<uint16_t *>(out);
-    p.ws_hdr = static_cast<int32_t *>(workspace);
-    p.ws_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan.hdr_bytes);
-    p.err_flag = err_flag;
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.MBS = MBS;
-    p.bs = bs;
-    p.NB = (int)NB;
-    p.stages = plan.stages;
-    p.scale_log2 = scale * 1.4426950408889634f;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = pkv::launch_decode(D, plan.NW, plan.G, &tmk, &tmv, p, plan.grid, plan.smem, s);
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+        return fail(PKV_ERR_INVALID_ARG, "store_kvcache_fp8: null pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return fail(PKV_ERR_INVALID_ARG, "store_kvcache_fp8: pointers must be 16-byte aligned");
+    const long long row = (long long)Hkv * D;
+    if (row > 0x7fffffffLL)
+        return fail(PKV_ERR_INVALID_ARG, "store_kvcache_fp8: row too large");
+    // The reciprocal is formed once here in IEEE fp32, so the kernel's
+    // products are exactly x * (1 / scale) rounded once.
+    const float kinv = 1.0f / k_scale, vinv = 1.0f / v_scale;
+    cudaError_t e = pkv::launch_store_fp8(k, v, k_cache, v_cache, slot_mapping, N, (int)row,
+                                          (long long)NB * bs, kinv, vinv, err_flag,
+                                          static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
-        return fail(PKV_ERR_CUDA, "paged_attn_decode launch: %s", cudaGetErrorString(e));
-    e = pkv::launch_merge(D, plan.G, p, s);
-    if (e != cudaSuccess)
-        return fail(PKV_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+        return fail(PKV_ERR_CUDA, "store_kvcache_fp8 launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }
 

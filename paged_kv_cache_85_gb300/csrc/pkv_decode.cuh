@@ -70,12 +70,13 @@ struct DecodeSmem {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int NW, int stages, int B)
+__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int NW, int stages, int B,
+                                                         int kv_elem_bytes = 2)
 {
     DecodeSmem L;
     size_t o = 0;
     L.kv = o;  // per stage: K boxes [NW][D/64][16][64], then V boxes alike (128B-swizzled rows)
-    o += (size_t)stages * 2 * NW * kBox * D * 2;
+    o += (size_t)stages * 2 * NW * kBox * D * kv_elem_bytes;
     L.q = o;  // per stage and worker: G query rows
     o = align_up(o + (size_t)stages * NW * G * D * 2, 16);
     L.full = o;
@@ -95,10 +96,11 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int NW, i
 }
 
 // Deepest pipeline (2..max_stages) whose shared memory fits max_smem.
-inline int decode_stages_for(int D, int G, int NW, int B, int max_stages, size_t max_smem)
+inline int decode_stages_for(int D, int G, int NW, int B, int max_stages, size_t max_smem,
+                             int kv_elem_bytes = 2)
 {
     for (int s = max_stages; s >= kMinStages; s--)
-        if (decode_smem_layout(D, G, NW, s, B).total <= max_smem)
+        if (decode_smem_layout(D, G, NW, s, B, kv_elem_bytes).total <= max_smem)
             return s;
     return 0;
 }
@@ -153,14 +155,14 @@ __device__ __forceinline__ int box_block(const DecodeParams &p, int b, int j)
 // register queue, so a copy never waits on a block-table read.  Per stage
 // every lane writes its worker's box descriptor and issues its own TMA
 // copies; lane 0 arms the stage's mbarrier with the summed byte count.
-template <int D, int G, int NW>
+template <int D, int G, int NW, bool F8>
 __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CUtensorMap *tmv,
                                                 const DecodeParams &p, uint8_t *smem,
                                                 const DecodeSmem &L, int lane, int R, int Tr,
                                                 int Wr, int P)
 {
     constexpr unsigned FULL = 0xffffffffu;
-    constexpr int kBoxBytes = kBox * D * 2;
+    constexpr int kBoxBytes = kBox * D * (F8 ? 1 : 2);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
     BoxMeta *meta = reinterpret_cast<BoxMeta *>(smem + L.meta);
@@ -261,7 +263,11 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
         if (flags & kPieceFirst)
             bulk_load(smem + L.q + ((size_t)stage * NW + lane) * G * D * 2,
                       p.q + ((size_t)b * p.Hq + (size_t)h * G) * D, G * D * 2, &full[stage]);
-        if (flags & kBoxLoaded) {
+        if ((flags & kBoxLoaded) && F8) {
+            uint8_t *kd = smem + L.kv + ((size_t)stage * 2 * NW + lane) * kBoxBytes;
+            tma_load_3d(kd, tmk, 0, h, row, &full[stage]);
+            tma_load_3d(kd + (size_t)NW * kBoxBytes, tmv, 0, h, row, &full[stage]);
+        } else if (flags & kBoxLoaded) {
             uint8_t *kd = smem + L.kv + ((size_t)stage * 2 * NW + lane) * kBoxBytes;
 #pragma unroll
             for (int half = 0; half < D / 64; half++) {
@@ -471,6 +477,208 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams &p, uint8_t *
     }
 }
 
+// Byte offset of 16-byte chunk `c` of row `t` in an FP8 box of 16 rows of D
+// bytes, as TMA writes it with the 128-byte (D = 128) or 64-byte (D = 64)
+// swizzle.
+template <int D> __device__ __forceinline__ uint32_t box8_chunk(int t, int c)
+{
+    if constexpr (D == 128)
+        return (uint32_t)(t * 128 + ((c ^ (t & 7)) << 4));
+    else
+        return (uint32_t)(t * 64 + ((c ^ ((t >> 1) & 3)) << 4));
+}
+
+// Consumer warp for FP8 (E4M3) caches.  Same pipeline and softmax as the
+// bf16 consumer; the MMAs run in f16 (E4M3 values are exact in f16; q is
+// converted to f16; P needs no hi/lo split with f16's 10 mantissa bits).
+// Fragments come from single 32-bit shared-memory loads by reindexing:
+//   * scores: the contraction index d is permuted inside each 16-wide
+//     k-step so that a lane's four B values (k = 2q, 2q+1, 8+2q, 9+2q) are
+//     the four consecutive bytes d = 16k + 4q .. +3 of its token row; q's A
+//     fragments use the same permutation, so S is unchanged;
+//   * P.V: output columns are permuted so that column c of n-tile 4g + r
+//     holds d = 32g + 4c + r; one 32-bit load of a V row then feeds four
+//     n-tiles, and each lane ends up owning 8 consecutive outputs per group.
+// K scales are folded into the score scale, V's scale into the output.
+template <int D, int G, int NW>
+__device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8_t *smem,
+                                                    const DecodeSmem &L, int warp, int lane)
+{
+    constexpr int KSTEPS = D / 16;
+    constexpr int NT = D / 8;
+    constexpr int NG = D / 32;       // groups of 4 n-tiles fed by one load per row
+    constexpr int kBoxBytes = kBox * D;
+    constexpr unsigned FULL = 0xffffffffu;
+
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
+    const BoxMeta *meta = reinterpret_cast<const BoxMeta *>(smem + L.meta);
+
+    const int hrow = lane >> 2;      // head row of the accumulators / token of K fragments
+    const int quad = lane & 3;
+    const bool real = hrow < G;
+    const int gw = blockIdx.x * NW + warp;
+
+    uint32_t qa[KSTEPS][2];
+    float o[NT][4];
+    float m_run = -INFINITY, l_run = 0.f;
+    bool whole = false;
+#pragma unroll
+    for (int k = 0; k < KSTEPS; k++)
+        qa[k][0] = qa[k][1] = 0u;
+#pragma unroll
+    for (int n = 0; n < NT; n++)
+        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+    int stage = 0;
+    uint32_t phase = 0;
+    for (;;) {
+        if (!__all_sync(FULL, mbar_wait(&full[stage], phase))) {
+            if (lane == 0)
+                flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
+            return;
+        }
+        const BoxMeta bm = meta[stage * NW + warp];
+        if (bm.flags & kStageStop)
+            break;
+        if (bm.flags & kPieceFirst) {
+            const uint8_t *qs = smem + L.q + ((size_t)stage * NW + warp) * G * D * 2;
+#pragma unroll
+            for (int k = 0; k < KSTEPS; k++) {
+                uint2 w = make_uint2(0u, 0u);
+                if (real)
+                    w = *reinterpret_cast<const uint2 *>(qs + (hrow * D + k * 16 + 4 * quad) * 2);
+                const float2 f01 = bf16x2_to_float2(w.x), f23 = bf16x2_to_float2(w.y);
+                qa[k][0] = pack_f16x2(f01.x, f01.y);
+                qa[k][1] = pack_f16x2(f23.x, f23.y);
+            }
+            m_run = -INFINITY;
+            l_run = 0.f;
+#pragma unroll
+            for (int n = 0; n < NT; n++)
+                o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            whole = (bm.flags & kStreamFirst) != 0;
+        }
+        const int nvw = (bm.flags & kBoxLoaded) ? bm.nvalid : 0;
+        if (nvw > 0) {
+            uint8_t *Ks = smem + L.kv + ((size_t)stage * 2 * NW + warp) * kBoxBytes;
+            uint8_t *Vs = Ks + (size_t)NW * kBoxBytes;
+            if (nvw < kBox) {
+                // Rows past the context take weight 0; 0 * NaN is still NaN on
+                // the tensor cores, so clear them (whole rows, any swizzle).
+                for (int i = lane; i < (kBox - nvw) * (D / 16); i += 32) {
+                    const int t = nvw + i / (D / 16), c = i % (D / 16);
+                    *reinterpret_cast<uint4 *>(Vs + t * D + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            // ---- scores ----
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int k = 0; k < KSTEPS; k++) {
+                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(Ks + box8_chunk<D>(hrow, k) + 4 * quad);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(Ks + box8_chunk<D>(hrow + 8, k) + 4 * quad);
+                mma_f16_16816(sc[0], qa[k][0], 0u, qa[k][1], 0u, e4m3x2_to_f16x2(w0),
+                              e4m3x2_to_f16x2(w0 >> 16));
+                mma_f16_16816(sc[1], qa[k][0], 0u, qa[k][1], 0u, e4m3x2_to_f16x2(w1),
+                              e4m3x2_to_f16x2(w1 >> 16));
+            }
+            // ---- online softmax (log2 domain) ----
+            float sv[4] = {sc[0][0], sc[0][1], sc[1][0], sc[1][1]};
+            const int tq = 2 * quad;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int t = tq + (i & 1) + ((i >> 1) << 3);
+                sv[i] = t < nvw ? sv[i] * p.scale_log2 : -INFINITY;
+            }
+            float mt = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+            mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 2));
+            const float m_new = fmaxf(m_run, mt);
+            const float alpha = fast_exp2(m_run - m_new);
+            m_run = m_new;
+            float pr[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                pr[i] = real ? fast_exp2(sv[i] - m_new) : 0.f;
+            l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+#pragma unroll
+            for (int n = 0; n < NT; n++) {
+                o[n][0] *= alpha;
+                o[n][1] *= alpha;
+            }
+            const uint32_t ph0 = pack_f16x2(pr[0], pr[1]);
+            const uint32_t ph2 = pack_f16x2(pr[2], pr[3]);
+            // ---- O += P V ----
+            const int c = hrow;  // this lane's column within every n-tile
+#pragma unroll
+            for (int g4 = 0; g4 < NG; g4++) {
+                const int chunk = 2 * g4 + (c >> 2);
+                const int wofs = 4 * (c & 3);
+                const uint32_t v0 = *reinterpret_cast<const uint32_t *>(Vs + box8_chunk<D>(tq, chunk) + wofs);
+                const uint32_t v1 = *reinterpret_cast<const uint32_t *>(Vs + box8_chunk<D>(tq + 1, chunk) + wofs);
+                const uint32_t v2 = *reinterpret_cast<const uint32_t *>(Vs + box8_chunk<D>(tq + 8, chunk) + wofs);
+                const uint32_t v3 = *reinterpret_cast<const uint32_t *>(Vs + box8_chunk<D>(tq + 9, chunk) + wofs);
+#pragma unroll
+                for (int r = 0; r < 4; r++) {
+                    const uint32_t sel = (uint32_t)(r | ((4 + r) << 4));
+                    const uint32_t b0 = e4m3x2_to_f16x2(prmt(v0, v1, sel));
+                    const uint32_t b1 = e4m3x2_to_f16x2(prmt(v2, v3, sel));
+                    mma_f16_16816(o[4 * g4 + r], ph0, 0u, ph2, 0u, b0, b1);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[stage]);
+
+        if (bm.flags & kPieceLast) {
+            float l_tot = l_run + __shfl_xor_sync(FULL, l_run, 1);
+            l_tot += __shfl_xor_sync(FULL, l_tot, 2);
+            const bool complete = whole && (bm.flags & kStreamLast);
+            if (real) {
+                const size_t hq = (size_t)bm.b * p.Hq + (size_t)bm.h * G + hrow;
+                if (complete) {
+                    const float f = l_tot > 0.f ? p.v_scale / l_tot : 0.f;
+#pragma unroll
+                    for (int g4 = 0; g4 < NG; g4++) {
+                        // outputs d = 32 g4 + 8 quad + 0..7
+                        const uint4 pk = make_uint4(
+                            pack_bf16x2(o[4 * g4 + 0][0] * f, o[4 * g4 + 1][0] * f),
+                            pack_bf16x2(o[4 * g4 + 2][0] * f, o[4 * g4 + 3][0] * f),
+                            pack_bf16x2(o[4 * g4 + 0][1] * f, o[4 * g4 + 1][1] * f),
+                            pack_bf16x2(o[4 * g4 + 2][1] * f, o[4 * g4 + 3][1] * f));
+                        *reinterpret_cast<uint4 *>(p.out + hq * D + 32 * g4 + 8 * quad) = pk;
+                    }
+                } else {
+                    float *pg = p.ws_part +
+                                (((size_t)gw * 2 + ((bm.flags & kSlot1) ? 1 : 0)) * G + hrow) * (D + 4);
+                    const float vs = p.v_scale;
+#pragma unroll
+                    for (int g4 = 0; g4 < NG; g4++) {
+                        float *dst = pg + 32 * g4 + 8 * quad;
+                        *reinterpret_cast<float4 *>(dst) =
+                            make_float4(o[4 * g4 + 0][0] * vs, o[4 * g4 + 1][0] * vs,
+                                        o[4 * g4 + 2][0] * vs, o[4 * g4 + 3][0] * vs);
+                        *reinterpret_cast<float4 *>(dst + 4) =
+                            make_float4(o[4 * g4 + 0][1] * vs, o[4 * g4 + 1][1] * vs,
+                                        o[4 * g4 + 2][1] * vs, o[4 * g4 + 3][1] * vs);
+                    }
+                    if (quad == 0) {
+                        pg[D] = m_run;
+                        pg[D + 1] = l_tot;
+                    }
+                }
+            }
+        }
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1;
+        }
+    }
+}
+
 // Per-sequence clamped lengths and the exclusive prefix sum of their box
 // counts (boxes per KV head before sequence b), b = 0..B.
 __device__ __forceinline__ void build_prefix(const DecodeParams &p, int *pb, int *len, int *wsum)
@@ -523,14 +731,14 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int *pb, int
     __syncthreads();
 }
 
-template <int D, int G, int NW>
+template <int D, int G, int NW, bool F8>
 __global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? 2 : 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const DecodeSmem L = decode_smem_layout(D, G, NW, p.stages, p.B);
+    const DecodeSmem L = decode_smem_layout(D, G, NW, p.stages, p.B, F8 ? 1 : 2);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -559,7 +767,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? 2 : 1)
     const int P = Tr > 0 ? (Tr + Wr - 1) / Wr : 1;
 
     if (warp == NW) {
-        decode_producer<D, G, NW>(&tmk, &tmv, p, smem, L, lane, R, Tr, Wr, P);
+        decode_producer<D, G, NW, F8>(&tmk, &tmv, p, smem, L, lane, R, Tr, Wr, P);
     } else {
         if (blockIdx.x == 0) {
             // Publish the box layout for the merge kernel (after the previous
@@ -575,11 +783,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? 2 : 1)
                 p.ws_hdr[4] = R;
             }
         }
-        decode_consumer<D, G, NW>(p, smem, L, warp, lane);
+        if constexpr (F8)
+            decode_consumer_fp8<D, G, NW>(p, smem, L, warp, lane);
+        else
+            decode_consumer<D, G, NW>(p, smem, L, warp, lane);
     }
 }
 
-template <int D, int NW>
+template <int D, int NW, bool F8>
 inline cudaError_t launch_decode_shape(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
                                        const DecodeParams &p, int grid, size_t smem,
                                        cudaStream_t stream)
@@ -595,21 +806,21 @@ inline cudaError_t launch_decode_shape(int G, const CUtensorMap *tmk, const CUte
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     switch (G) {
-    case 1: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 1, NW>, *tmk, *tmv, p);
-    case 2: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 2, NW>, *tmk, *tmv, p);
-    case 4: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 4, NW>, *tmk, *tmv, p);
-    case 8: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 8, NW>, *tmk, *tmv, p);
+    case 1: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 1, NW, F8>, *tmk, *tmv, p);
+    case 2: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 2, NW, F8>, *tmk, *tmv, p);
+    case 4: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 4, NW, F8>, *tmk, *tmv, p);
+    case 8: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 8, NW, F8>, *tmk, *tmv, p);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int D, int NW> inline const void *decode_kernel_shape(int G)
+template <int D, int NW, bool F8> inline const void *decode_kernel_shape(int G)
 {
     switch (G) {
-    case 1: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 1, NW>);
-    case 2: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 2, NW>);
-    case 4: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 4, NW>);
-    case 8: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 8, NW>);
+    case 1: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 1, NW, F8>);
+    case 2: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 2, NW, F8>);
+    case 4: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 4, NW, F8>);
+    case 8: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 8, NW, F8>);
     default: return nullptr;
     }
 }

@@ -1,5 +1,5 @@
 // Instantiations of the paged decode kernel: head_dim 128, 8 workers per CTA,
-// G = 1, 2, 4, 8.
+// bf16 caches, G = 1, 2, 4, 8.
 #include "pkv_decode.cuh"
 
 namespace pkv {
@@ -7,9 +7,9 @@ namespace pkv {
 cudaError_t launch_decode_d128_w8(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
                                  const DecodeParams &p, int grid, size_t smem, cudaStream_t stream)
 {
-    return launch_decode_shape<128, 8>(G, tmk, tmv, p, grid, smem, stream);
+    return launch_decode_shape<128, 8, false>(G, tmk, tmv, p, grid, smem, stream);
 }
 
-const void *decode_kernel_d128_w8(int G) { return decode_kernel_shape<128, 8>(G); }
+const void *decode_kernel_d128_w8(int G) { return decode_kernel_shape<128, 8, false>(G); }
 
 } // namespace pkv

@@ -1,5 +1,5 @@
 // Instantiations of the paged decode kernel: head_dim 64, 4 workers per CTA,
-// G = 1, 2, 4, 8.
+// bf16 caches, G = 1, 2, 4, 8.
 #include "pkv_decode.cuh"
 
 namespace pkv {
@@ -7,9 +7,9 @@ namespace pkv {
 cudaError_t launch_decode_d64_w4(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
                                  const DecodeParams &p, int grid, size_t smem, cudaStream_t stream)
 {
-    return launch_decode_shape<64, 4>(G, tmk, tmv, p, grid, smem, stream);
+    return launch_decode_shape<64, 4, false>(G, tmk, tmv, p, grid, smem, stream);
 }
 
-const void *decode_kernel_d64_w4(int G) { return decode_kernel_shape<64, 4>(G); }
+const void *decode_kernel_d64_w4(int G) { return decode_kernel_shape<64, 4, false>(G); }
 
 } // namespace pkv

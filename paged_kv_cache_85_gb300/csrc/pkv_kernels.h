@@ -39,13 +39,18 @@ struct DecodeParams {
     int B, Hq, Hkv, MBS, bs;
     int NB;
     int stages;                   // pipeline depth chosen on the host to fit shared memory
-    float scale_log2;             // scale * log2(e)
+    float scale_log2;             // scale * log2(e) (FP8 caches: times k_scale)
+    float v_scale;                // FP8 caches: dequant scale of V (1 for bf16)
 };
 
 // Host launchers (defined next to their kernels).
 cudaError_t launch_store(const void *k, const void *v, void *k_cache, void *v_cache,
                          const int64_t *slot_mapping, int64_t N, int row_bytes,
                          long long n_slots, int32_t *err_flag, cudaStream_t stream);
+cudaError_t launch_store_fp8(const void *k, const void *v, void *k_cache, void *v_cache,
+                             const int64_t *slot_mapping, int64_t N, int row_elems,
+                             long long n_slots, float kinv, float vinv, int32_t *err_flag,
+                             cudaStream_t stream);
 cudaError_t launch_merge(int D, int G, const DecodeParams &p, cudaStream_t stream);
 
 } // namespace pkv

@@ -85,9 +85,10 @@ class Workload:
     def N(self) -> int:
         return int(self.slot_mapping.shape[0])
 
-    def kv_bytes(self) -> int:
-        """K and V bytes over every sequence's context (logical)."""
-        return int(self.context_lens.astype(np.int64).sum()) * self.Hkv * self.D * 2 * 2
+    def kv_bytes(self, elem_bytes: int = 2) -> int:
+        """K and V bytes over every sequence's context (logical); 1 byte per
+        element for an FP8 cache."""
+        return int(self.context_lens.astype(np.int64).sum()) * self.Hkv * self.D * elem_bytes * 2
 
     def unique_kv_bytes(self) -> int:
         """K and V bytes of the distinct physical blocks the step reads."""
@@ -103,15 +104,16 @@ class Workload:
                 tok += min(self.bs, n - j * self.bs)
         return tok * self.Hkv * self.D * 2 * 2
 
-    def decode_bytes(self) -> int:
+    def decode_bytes(self, kv_elem_bytes: int = 2) -> int:
         """Algorithmic bytes of one decode: K/V over context + q + out + table + lens."""
         tables = sum((int(n) + self.bs - 1) // self.bs for n in self.context_lens) * 4
-        return self.kv_bytes() + 2 * self.B * self.Hq * self.D * 2 + tables + 4 * self.B
+        return self.kv_bytes(kv_elem_bytes) + 2 * self.B * self.Hq * self.D * 2 + tables + 4 * self.B
 
-    def store_bytes(self) -> int:
-        """Algorithmic bytes of one store: valid rows read + written, plus slots."""
+    def store_bytes(self, kv_elem_bytes: int = 2) -> int:
+        """Algorithmic bytes of one store: valid bf16 rows read, cache rows
+        written (kv_elem_bytes per element), plus slots."""
         nv = int((self.slot_mapping >= 0).sum())
-        return 2 * nv * self.Hkv * self.D * 2 * 2 + 8 * self.N
+        return nv * self.Hkv * self.D * (2 + kv_elem_bytes) * 2 + 8 * self.N
 
 
 def decode_slot(block_table_row: np.ndarray, ctx: int, bs: int) -> int:

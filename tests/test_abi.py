@@ -47,14 +47,13 @@ def test_host_only_entry_points(cuda_lib_path):
     f.restype = ctypes.c_size_t
     f.argtypes = [ctypes.c_int] * 7
     hdr = lambda B: (8 + B + 1) * 4 + (-(8 + B + 1) * 4) % 256
-    # 4 seqs x 2 KV heads x 19 boxes = 152 boxes -> 38 CTAs of 4 workers (two CTAs fit an SM);
-    # two partial slots per worker of G x (D + 4) floats
-    assert f(4, 4, 2, 64, 19, 16, 0) == hdr(4) + 38 * 4 * 2 * 2 * 68 * 4
-    # large problems: capped at 2048 workers; max_ctas caps further
-    assert f(64, 16, 8, 128, 16, 256, 0) == hdr(64) + 512 * 4 * 2 * 2 * 132 * 4
-    assert f(64, 16, 8, 128, 16, 256, 10) == hdr(64) + 10 * 4 * 2 * 2 * 132 * 4
-    # G = 8 at D = 128 does not fit two CTAs per SM: 8-worker CTAs
-    assert f(64, 64, 8, 128, 16, 256, 10) == hdr(64) + 10 * 8 * 2 * 8 * 132 * 4
+    # Two partial slots of G x (D + 4) floats per worker; workers are bounded by
+    # boxes + 7 (4 seqs x 2 KV heads x 19 boxes = 152 boxes -> 159), by 2048, and by
+    # max_ctas CTAs of up to 8 workers.
+    assert f(4, 4, 2, 64, 19, 16, 0) == hdr(4) + 159 * 2 * 2 * 68 * 4
+    assert f(64, 16, 8, 128, 16, 256, 0) == hdr(64) + 2048 * 2 * 2 * 132 * 4
+    assert f(64, 16, 8, 128, 16, 256, 10) == hdr(64) + 80 * 2 * 2 * 132 * 4
+    assert f(64, 64, 8, 128, 16, 256, 10) == hdr(64) + 80 * 2 * 8 * 132 * 4
     assert f(-1, 4, 2, 64, 19, 16, 0) == 0
     assert f(0, 4, 2, 64, 19, 16, 0) == 0
     assert f(4, 6, 4, 64, 19, 16, 0) == 0  # Hq not a multiple of Hkv
@@ -90,3 +89,30 @@ def test_argument_errors_need_no_gpu(cuda_lib_path):
     lib.pkv_store_kvcache.argtypes = [P, P, P, P, P, i64, i32, i32, i64, i32, P, P]
     assert lib.pkv_store_kvcache(None, None, None, None, None, 0, 2, 64, 4, 16, None, None) == 0
     assert lib.pkv_store_kvcache(None, None, None, None, None, 3, 2, 64, 4, 16, None, None) == 1
+
+
+def test_fp8_argument_errors_need_no_gpu(cuda_lib_path):
+    lib = ctypes.CDLL(cuda_lib_path)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.pkv_last_error.restype = ctypes.c_char_p
+    st8 = lib.pkv_store_kvcache_fp8
+    st8.restype = i32
+    st8.argtypes = [P, P, P, P, P, i64, i32, i32, i64, i32, f32, f32, P, P]
+    assert st8(None, None, None, None, None, 0, 2, 64, 4, 16, 1.0, 1.0, None, None) == 0
+    assert st8(None, None, None, None, None, 0, 1, 8, 4, 16, 1.0, 1.0, None, None) == 2  # Hkv*D % 16
+    assert st8(None, None, None, None, None, 0, 2, 64, 4, 16, 0.0, 1.0, None, None) == 1
+    assert st8(None, None, None, None, None, 0, 2, 64, 4, 16, 1.0, float("nan"), None, None) == 1
+    assert b"scales" in lib.pkv_last_error()
+    assert st8(None, None, None, None, None, 3, 2, 64, 4, 16, 1.0, 1.0, None, None) == 1  # null
+    dec8 = lib.pkv_paged_attn_decode_fp8
+    dec8.restype = i32
+    dec8.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32, f32, f32, f32, P, P, sz, i32,
+                     P, P]
+    assert dec8(None, None, None, None, 1, None, 1, 6, 4, 64, 1, 16, 1.0, 1.0, 1.0,
+                None, None, 0, 0, None, None) == 1
+    assert dec8(None, None, None, None, 1, None, 1, 4, 4, 96, 1, 16, 1.0, 1.0, 1.0,
+                None, None, 0, 0, None, None) == 2
+    assert dec8(None, None, None, None, 1, None, 1, 4, 4, 64, 1, 16, 1.0, -1.0, 1.0,
+                None, None, 0, 0, None, None) == 1
+    assert dec8(None, None, None, None, 1, None, 0, 4, 4, 64, 1, 16, 1.0, 1.0, 1.0,
+                None, None, 0, 0, None, None) == 0

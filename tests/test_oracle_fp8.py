@@ -108,3 +108,15 @@ def test_fp8_decode_scales_are_applied():
     np.testing.assert_allclose(vs, 0.25 * base, rtol=1e-14)
     ks = oracle.paged_attn_decode_fp8(q, codes, codes, tables, lens, 0.25, 2.0, 1.0)
     np.testing.assert_allclose(ks, base, rtol=1e-13)  # scale 0.25 * k_scale 2 == scale 0.5
+
+
+def test_table_quantizer_equals_the_plain_store():
+    """The memoised quantizer gives the plain store's codes for every input."""
+    rng = np.random.default_rng(3)
+    bits = rng.integers(0, 65536, size=(40, 2, 64)).astype(np.uint16)
+    slots = np.arange(40, dtype=np.int64)
+    cache = np.zeros((10, 4, 2, 64), np.uint8)
+    for scale in (1.0, 0.0137, 3.7):
+        kc, vc, bad = oracle.store_kvcache_fp8(bits, bits, cache, cache, slots, scale, scale)
+        assert bad == 0
+        np.testing.assert_array_equal(oracle.quantize_bf16(bits, scale), kc.reshape(40, 2, 64))
