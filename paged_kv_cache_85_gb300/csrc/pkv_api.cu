@@ -280,12 +280,18 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
     const long long box_max = (long long)B * Hkv * (((long long)MBS * bs + pkv::kBox - 1) / pkv::kBox);
     if (box_max >= 0x7fffffffLL)
         return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: B*Hkv*MBS*bs/16 must be < 2^31");
-    // Prefer two 4-worker CTAs per SM; fall back to one 8-worker CTA per SM
-    // when two do not fit (large B, or G = 8 with D = 128).
+    // Prefer 4-worker CTAs, three per SM for FP8 caches (their kernels are
+    // built for three) and two for bf16; fall back to one 8-worker CTA per
+    // SM when they do not fit (large B, or G = 8 with D = 128).
     const size_t pair_smem = pkv::kSmemPerSm / 2 - pkv::kSmemReserve;
+    const size_t trio_smem = pkv::kSmemPerSm / 3 - pkv::kSmemReserve;
     const int eb = f8 ? 1 : 2;  // bytes per cached element
     int NW = pkv::kPairWorkers;
-    int stages = pkv::decode_stages_for(D, G, NW, B, pkv::kPairStages, pair_smem, eb);
+    int stages = 0;
+    if (f8)
+        stages = pkv::decode_stages_for(D, G, NW, B, pkv::kPairStages, trio_smem, eb);
+    if (stages < pkv::kPairStages)
+        stages = pkv::decode_stages_for(D, G, NW, B, pkv::kPairStages, pair_smem, eb);
     if (stages < pkv::kPairStages) {
         NW = pkv::kWideWorkers;
         stages = pkv::decode_stages_for(D, G, NW, B, pkv::kMaxStages, kMaxDynSmem, eb);

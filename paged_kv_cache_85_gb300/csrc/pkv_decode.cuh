@@ -488,47 +488,72 @@ template <int D> __device__ __forceinline__ uint32_t box8_chunk(int t, int c)
         return (uint32_t)(t * 64 + ((c ^ ((t >> 1) & 3)) << 4));
 }
 
-// Consumer warp for FP8 (E4M3) caches.  Same pipeline and softmax as the
-// bf16 consumer; the MMAs run in f16 (E4M3 values are exact in f16; q is
-// converted to f16; P needs no hi/lo split with f16's 10 mantissa bits).
-// Fragments come from single 32-bit shared-memory loads by reindexing:
-//   * scores: the contraction index d is permuted inside each 16-wide
-//     k-step so that a lane's four B values (k = 2q, 2q+1, 8+2q, 9+2q) are
-//     the four consecutive bytes d = 16k + 4q .. +3 of its token row; q's A
-//     fragments use the same permutation, so S is unchanged;
-//   * P.V: output columns are permuted so that column c of n-tile 4g + r
-//     holds d = 32g + 4c + r; one 32-bit load of a V row then feeds four
-//     n-tiles, and each lane ends up owning 8 consecutive outputs per group.
-// K scales are folded into the score scale, V's scale into the output.
+// Consumer warp for FP8 (E4M3) caches.  Same pipeline, slices and outputs as
+// the bf16 consumer; the arithmetic is arranged around the 8-bit data:
+//   * scores S^T = K q^T run on the E4M3 tensor-core path (m16n8k32) with the
+//     box's 16 tokens as M and the group's heads as N, so K fragments are
+//     the raw codes read from shared memory, four per 32-bit word.  q enters
+//     as two E4M3 parts under a power-of-two scale per head, q = sq (hi +
+//     lo / 16): hi is q / sq rounded to E4M3 and lo the remainder times 16,
+//     which represents every bf16 element of magnitude >= max|q| 2^-14
+//     exactly (the rest to within max|q| 2^-21).  The contraction index is
+//     permuted so that each lane's bytes are one contiguous run of its row;
+//   * P.V runs as O^T = V^T P^T in f16 (m16n8k16) with head dimension d as
+//     M: E4M3 values are exact in f16, P is rounded to f16, and P^T's
+//     fragments come from the score accumulators by one movmatrix transpose.
+//     d is permuted so that a lane reads D/8 contiguous bytes of a token row
+//     and owns D/8 contiguous outputs per head;
+//   * the running max is only moved (and O, l rescaled) when a head's box
+//     max exceeds it by more than 2^8, which bounds P by 256 (exact range of
+//     f16) and skips the rescale on most boxes.
+// k_scale is folded into the score scale and v_scale into the output.
 template <int D, int G, int NW>
 __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8_t *smem,
                                                     const DecodeSmem &L, int warp, int lane)
 {
-    constexpr int KSTEPS = D / 16;
-    constexpr int NT = D / 8;
-    constexpr int NG = D / 32;       // groups of 4 n-tiles fed by one load per row
+    constexpr int KS = D / 32;   // k-steps of the score MMA
+    constexpr int KW = D / 16;   // K words per lane per token row (D/4 bytes)
+    constexpr int MT = D / 16;   // m-tiles of O^T
+    constexpr int VW = D / 32;   // V words per lane per token row (D/8 bytes)
     constexpr int kBoxBytes = kBox * D;
     constexpr unsigned FULL = 0xffffffffu;
+    constexpr float kLazy = 8.f;
 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
     const BoxMeta *meta = reinterpret_cast<const BoxMeta *>(smem + L.meta);
 
-    const int hrow = lane >> 2;      // head row of the accumulators / token of K fragments
-    const int quad = lane & 3;
-    const bool real = hrow < G;
+    const int g = lane >> 2;     // token row of S^T, head of q's B fragments, d-group of V
+    const int quad = lane & 3;   // heads 2quad, 2quad+1 of S^T and O^T; token pair of V
+    const int h0 = 2 * quad, h1 = 2 * quad + 1;
     const int gw = blockIdx.x * NW + warp;
 
-    uint32_t qa[KSTEPS][2];
-    float o[NT][4];
-    float m_run = -INFINITY, l_run = 0.f;
+    // shared-memory offsets of this lane's bytes within a box
+    uint32_t koff[2][KW / 4];    // rows g, g+8: 16-byte chunks quad*(D/64) + c
+#pragma unroll
+    for (int c = 0; c < KW / 4; c++) {
+        koff[0][c] = box8_chunk<D>(g, quad * (KW / 4) + c);
+        koff[1][c] = box8_chunk<D>(g + 8, quad * (KW / 4) + c);
+    }
+    uint32_t voff[4];            // rows 2quad, 2quad+1, 2quad+8, 2quad+9 at byte g*D/8
+    {
+        const int rows[4] = {h0, h1, h0 + 8, h1 + 8};
+#pragma unroll
+        for (int r = 0; r < 4; r++)
+            voff[r] = box8_chunk<D>(rows[r], (g * (D / 8)) >> 4) + ((g * (D / 8)) & 15);
+    }
+
+    uint32_t qh[KW], ql[KW];
+    float f0 = 0.f, f0l = 0.f, f1 = 0.f, f1l = 0.f;
+    float o[MT][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     bool whole = false;
 #pragma unroll
-    for (int k = 0; k < KSTEPS; k++)
-        qa[k][0] = qa[k][1] = 0u;
+    for (int j = 0; j < MT; j++)
+        o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 #pragma unroll
-    for (int n = 0; n < NT; n++)
-        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int w = 0; w < KW; w++)
+        qh[w] = ql[w] = 0u;
 
     int stage = 0;
     uint32_t phase = 0;
@@ -542,90 +567,149 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8
         if (bm.flags & kStageStop)
             break;
         if (bm.flags & kPieceFirst) {
+            // q of head g, d in [quad*D/4, +D/4), split into E4M3 hi / lo
             const uint8_t *qs = smem + L.q + ((size_t)stage * NW + warp) * G * D * 2;
+            float x[D / 4];
 #pragma unroll
-            for (int k = 0; k < KSTEPS; k++) {
-                uint2 w = make_uint2(0u, 0u);
-                if (real)
-                    w = *reinterpret_cast<const uint2 *>(qs + (hrow * D + k * 16 + 4 * quad) * 2);
-                const float2 f01 = bf16x2_to_float2(w.x), f23 = bf16x2_to_float2(w.y);
-                qa[k][0] = pack_f16x2(f01.x, f01.y);
-                qa[k][1] = pack_f16x2(f23.x, f23.y);
+            for (int c = 0; c < D / 32; c++) {
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (g < G)
+                    w = *reinterpret_cast<const uint4 *>(qs + (g * D + quad * (D / 4) + 8 * c) * 2);
+                const float2 a = bf16x2_to_float2(w.x), b = bf16x2_to_float2(w.y);
+                const float2 e = bf16x2_to_float2(w.z), f = bf16x2_to_float2(w.w);
+                x[8 * c + 0] = a.x; x[8 * c + 1] = a.y; x[8 * c + 2] = b.x; x[8 * c + 3] = b.y;
+                x[8 * c + 4] = e.x; x[8 * c + 5] = e.y; x[8 * c + 6] = f.x; x[8 * c + 7] = f.y;
             }
-            m_run = -INFINITY;
-            l_run = 0.f;
+            float amax = 0.f;
 #pragma unroll
-            for (int n = 0; n < NT; n++)
-                o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            for (int i = 0; i < D / 4; i++)
+                amax = fmaxf(amax, fabsf(x[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
+            // sq = 2^(E - 7) for amax in [2^E, 2^(E+1)): |q / sq| < 256 <= 448
+            int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+            ebits = min(max(ebits, 8), 254);
+            const float sq = __uint_as_float((uint32_t)(ebits - 7) << 23);
+            const float inv = __uint_as_float((uint32_t)(261 - ebits) << 23);
+#pragma unroll
+            for (int w = 0; w < KW; w++) {
+                float xs[4], rs[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    xs[i] = x[4 * w + i] * inv;
+                const uint32_t c01 = f32x2_to_e4m3x2(xs[0], xs[1]);
+                const uint32_t c23 = f32x2_to_e4m3x2(xs[2], xs[3]);
+                const float2 b01 = f16x2_to_float2(e4m3x2_to_f16x2(c01));
+                const float2 b23 = f16x2_to_float2(e4m3x2_to_f16x2(c23));
+                rs[0] = (xs[0] - b01.x) * 16.f;
+                rs[1] = (xs[1] - b01.y) * 16.f;
+                rs[2] = (xs[2] - b23.x) * 16.f;
+                rs[3] = (xs[3] - b23.y) * 16.f;
+                qh[w] = c01 | (c23 << 16);
+                ql[w] = f32x2_to_e4m3x2(rs[0], rs[1]) | (f32x2_to_e4m3x2(rs[2], rs[3]) << 16);
+            }
+            const float sq0 = __shfl_sync(FULL, sq, 4 * h0);
+            const float sq1 = __shfl_sync(FULL, sq, (4 * h1) & 31);
+            f0 = p.scale_log2 * sq0;
+            f1 = p.scale_log2 * sq1;
+            f0l = f0 * 0.0625f;
+            f1l = f1 * 0.0625f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < MT; j++)
+                o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
             whole = (bm.flags & kStreamFirst) != 0;
         }
         const int nvw = (bm.flags & kBoxLoaded) ? bm.nvalid : 0;
         if (nvw > 0) {
-            uint8_t *Ks = smem + L.kv + ((size_t)stage * 2 * NW + warp) * kBoxBytes;
-            uint8_t *Vs = Ks + (size_t)NW * kBoxBytes;
-            if (nvw < kBox) {
-                // Rows past the context take weight 0; 0 * NaN is still NaN on
-                // the tensor cores, so clear them (whole rows, any swizzle).
-                for (int i = lane; i < (kBox - nvw) * (D / 16); i += 32) {
-                    const int t = nvw + i / (D / 16), c = i % (D / 16);
-                    *reinterpret_cast<uint4 *>(Vs + t * D + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            const uint8_t *Ks = smem + L.kv + ((size_t)stage * 2 * NW + warp) * kBoxBytes;
+            const uint8_t *Vs = Ks + (size_t)NW * kBoxBytes;
+            // ---- scores S^T (tokens g, g+8; heads h0, h1) ----
+            uint32_t ka[2][KW];
+#pragma unroll
+            for (int r = 0; r < 2; r++)
+#pragma unroll
+                for (int c = 0; c < KW / 4; c++) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(Ks + koff[r][c]);
+                    ka[r][4 * c + 0] = w.x;
+                    ka[r][4 * c + 1] = w.y;
+                    ka[r][4 * c + 2] = w.z;
+                    ka[r][4 * c + 3] = w.w;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
+            float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < KS; k++) {
+                mma_e4m3_16832(sh, ka[0][2 * k], ka[1][2 * k], ka[0][2 * k + 1], ka[1][2 * k + 1],
+                               qh[2 * k], qh[2 * k + 1]);
+                mma_e4m3_16832(sl, ka[0][2 * k], ka[1][2 * k], ka[0][2 * k + 1], ka[1][2 * k + 1],
+                               ql[2 * k], ql[2 * k + 1]);
             }
-            // ---- scores ----
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float sv[4] = {fmaf(sl[0], f0l, sh[0] * f0), fmaf(sl[1], f1l, sh[1] * f1),
+                           fmaf(sl[2], f0l, sh[2] * f0), fmaf(sl[3], f1l, sh[3] * f1)};
+            // V words of tokens 2quad, 2quad+1, 2quad+8, 2quad+9
+            uint32_t vw[4][VW];
 #pragma unroll
-            for (int k = 0; k < KSTEPS; k++) {
-                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(Ks + box8_chunk<D>(hrow, k) + 4 * quad);
-                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(Ks + box8_chunk<D>(hrow + 8, k) + 4 * quad);
-                mma_f16_16816(sc[0], qa[k][0], 0u, qa[k][1], 0u, e4m3x2_to_f16x2(w0),
-                              e4m3x2_to_f16x2(w0 >> 16));
-                mma_f16_16816(sc[1], qa[k][0], 0u, qa[k][1], 0u, e4m3x2_to_f16x2(w1),
-                              e4m3x2_to_f16x2(w1 >> 16));
+            for (int r = 0; r < 4; r++) {
+                if constexpr (VW == 4) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(Vs + voff[r]);
+                    vw[r][0] = w.x; vw[r][1] = w.y; vw[r][2] = w.z; vw[r][3] = w.w;
+                } else {
+                    const uint2 w = *reinterpret_cast<const uint2 *>(Vs + voff[r]);
+                    vw[r][0] = w.x; vw[r][1] = w.y;
+                }
             }
-            // ---- online softmax (log2 domain) ----
-            float sv[4] = {sc[0][0], sc[0][1], sc[1][0], sc[1][1]};
-            const int tq = 2 * quad;
+            if (nvw < kBox) {
+                // tokens past the context: scores -inf, V 0 (0 * NaN is NaN)
+                if (g >= nvw) { sv[0] = -INFINITY; sv[1] = -INFINITY; }
+                if (g + 8 >= nvw) { sv[2] = -INFINITY; sv[3] = -INFINITY; }
+                const int rows[4] = {h0, h1, h0 + 8, h1 + 8};
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const int t = tq + (i & 1) + ((i >> 1) << 3);
-                sv[i] = t < nvw ? sv[i] * p.scale_log2 : -INFINITY;
+                for (int r = 0; r < 4; r++)
+                    if (rows[r] >= nvw) {
+#pragma unroll
+                        for (int w = 0; w < VW; w++)
+                            vw[r][w] = 0u;
+                    }
             }
-            float mt = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-            mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 1));
-            mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 2));
-            const float m_new = fmaxf(m_run, mt);
-            const float alpha = fast_exp2(m_run - m_new);
-            m_run = m_new;
-            float pr[4];
+            // ---- online softmax per head column (log2 domain) ----
+            float b0 = fmaxf(sv[0], sv[2]), b1 = fmaxf(sv[1], sv[3]);
 #pragma unroll
-            for (int i = 0; i < 4; i++)
-                pr[i] = real ? fast_exp2(sv[i] - m_new) : 0.f;
-            l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-#pragma unroll
-            for (int n = 0; n < NT; n++) {
-                o[n][0] *= alpha;
-                o[n][1] *= alpha;
+            for (int x = 4; x < 32; x <<= 1) {
+                b0 = fmaxf(b0, __shfl_xor_sync(FULL, b0, x));
+                b1 = fmaxf(b1, __shfl_xor_sync(FULL, b1, x));
             }
-            const uint32_t ph0 = pack_f16x2(pr[0], pr[1]);
-            const uint32_t ph2 = pack_f16x2(pr[2], pr[3]);
-            // ---- O += P V ----
-            const int c = hrow;  // this lane's column within every n-tile
+            if (__any_sync(FULL, b0 > m0 + kLazy || b1 > m1 + kLazy)) {
+                const float n0 = fmaxf(m0, b0), n1 = fmaxf(m1, b1);
+                const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);
+                m0 = n0;
+                m1 = n1;
+                l0 *= a0;
+                l1 *= a1;
 #pragma unroll
-            for (int g4 = 0; g4 < NG; g4++) {
-                const int chunk = 2 * g4 + (c >> 2);
-                const int wofs = 4 * (c & 3);
-                const uint32_t v0 = *reinterpret_cast<const uint32_t *>(Vs + box8_chunk<D>(tq, chunk) + wofs);
-                const uint32_t v1 = *reinterpret_cast<const uint32_t *>(Vs + box8_chunk<D>(tq + 1, chunk) + wofs);
-                const uint32_t v2 = *reinterpret_cast<const uint32_t *>(Vs + box8_chunk<D>(tq + 8, chunk) + wofs);
-                const uint32_t v3 = *reinterpret_cast<const uint32_t *>(Vs + box8_chunk<D>(tq + 9, chunk) + wofs);
+                for (int j = 0; j < MT; j++) {
+                    o[j][0] *= a0;
+                    o[j][1] *= a1;
+                    o[j][2] *= a0;
+                    o[j][3] *= a1;
+                }
+            }
+            const float p0 = fast_exp2(sv[0] - m0), p1 = fast_exp2(sv[1] - m1);
+            const float p2 = fast_exp2(sv[2] - m0), p3 = fast_exp2(sv[3] - m1);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
+            const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
+            // ---- O^T += V^T P^T ----
 #pragma unroll
-                for (int r = 0; r < 4; r++) {
-                    const uint32_t sel = (uint32_t)(r | ((4 + r) << 4));
-                    const uint32_t b0 = e4m3x2_to_f16x2(prmt(v0, v1, sel));
-                    const uint32_t b1 = e4m3x2_to_f16x2(prmt(v2, v3, sel));
-                    mma_f16_16816(o[4 * g4 + r], ph0, 0u, ph2, 0u, b0, b1);
+            for (int w = 0; w < VW; w++) {
+                uint32_t a[2][4];  // [m-tile 2w + i][a0..a3]
+#pragma unroll
+                for (int i = 0; i < 2; i++) {
+                    const uint32_t sel = i == 0 ? 0x5140u : 0x7362u;
+                    e4m3x4_to_f16x2x2(prmt(vw[0][w], vw[1][w], sel), a[i][0], a[i][1]);
+                    e4m3x4_to_f16x2x2(prmt(vw[2][w], vw[3][w], sel), a[i][2], a[i][3]);
+                    mma_f16_16816(o[2 * w + i], a[i][0], a[i][1], a[i][2], a[i][3], pb0, pb1);
                 }
             }
         }
@@ -634,40 +718,49 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8
             mbar_arrive(&empty[stage]);
 
         if (bm.flags & kPieceLast) {
-            float l_tot = l_run + __shfl_xor_sync(FULL, l_run, 1);
-            l_tot += __shfl_xor_sync(FULL, l_tot, 2);
-            const bool complete = whole && (bm.flags & kStreamLast);
-            if (real) {
-                const size_t hq = (size_t)bm.b * p.Hq + (size_t)bm.h * G + hrow;
-                if (complete) {
-                    const float f = l_tot > 0.f ? p.v_scale / l_tot : 0.f;
+            float t0 = l0, t1 = l1;
 #pragma unroll
-                    for (int g4 = 0; g4 < NG; g4++) {
-                        // outputs d = 32 g4 + 8 quad + 0..7
-                        const uint4 pk = make_uint4(
-                            pack_bf16x2(o[4 * g4 + 0][0] * f, o[4 * g4 + 1][0] * f),
-                            pack_bf16x2(o[4 * g4 + 2][0] * f, o[4 * g4 + 3][0] * f),
-                            pack_bf16x2(o[4 * g4 + 0][1] * f, o[4 * g4 + 1][1] * f),
-                            pack_bf16x2(o[4 * g4 + 2][1] * f, o[4 * g4 + 3][1] * f));
-                        *reinterpret_cast<uint4 *>(p.out + hq * D + 32 * g4 + 8 * quad) = pk;
+            for (int x = 4; x < 32; x <<= 1) {
+                t0 += __shfl_xor_sync(FULL, t0, x);
+                t1 += __shfl_xor_sync(FULL, t1, x);
+            }
+            const bool complete = whole && (bm.flags & kStreamLast);
+            const size_t hq0 = (size_t)bm.b * p.Hq + (size_t)bm.h * G;
+            // this lane owns d = g*D/8 + 0 .. D/8-1 of heads h0 (o[.][0], o[.][2]) and h1
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                const int head = hh == 0 ? h0 : h1;
+                if (head >= G)
+                    continue;
+                const float lt = hh == 0 ? t0 : t1;
+                const float mr = hh == 0 ? m0 : m1;
+                if (complete) {
+                    const float f = lt > 0.f ? p.v_scale / lt : 0.f;
+                    uint16_t *dst = p.out + (hq0 + head) * D + g * (D / 8);
+#pragma unroll
+                    for (int c = 0; c < D / 64; c++) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const int j = 4 * c + i;
+                            pk[i] = pack_bf16x2(o[j][hh] * f, o[j][2 + hh] * f);
+                        }
+                        *reinterpret_cast<uint4 *>(dst + 8 * c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     }
                 } else {
                     float *pg = p.ws_part +
-                                (((size_t)gw * 2 + ((bm.flags & kSlot1) ? 1 : 0)) * G + hrow) * (D + 4);
+                                (((size_t)gw * 2 + ((bm.flags & kSlot1) ? 1 : 0)) * G + head) * (D + 4);
                     const float vs = p.v_scale;
 #pragma unroll
-                    for (int g4 = 0; g4 < NG; g4++) {
-                        float *dst = pg + 32 * g4 + 8 * quad;
-                        *reinterpret_cast<float4 *>(dst) =
-                            make_float4(o[4 * g4 + 0][0] * vs, o[4 * g4 + 1][0] * vs,
-                                        o[4 * g4 + 2][0] * vs, o[4 * g4 + 3][0] * vs);
-                        *reinterpret_cast<float4 *>(dst + 4) =
-                            make_float4(o[4 * g4 + 0][1] * vs, o[4 * g4 + 1][1] * vs,
-                                        o[4 * g4 + 2][1] * vs, o[4 * g4 + 3][1] * vs);
+                    for (int c = 0; c < D / 32; c++) {
+                        const int j = 2 * c;
+                        *reinterpret_cast<float4 *>(pg + g * (D / 8) + 4 * c) =
+                            make_float4(o[j][hh] * vs, o[j][2 + hh] * vs, o[j + 1][hh] * vs,
+                                        o[j + 1][2 + hh] * vs);
                     }
-                    if (quad == 0) {
-                        pg[D] = m_run;
-                        pg[D + 1] = l_tot;
+                    if (g == 0) {
+                        pg[D] = mr;
+                        pg[D + 1] = lt;
                     }
                 }
             }
@@ -732,7 +825,7 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int *pb, int
 }
 
 template <int D, int G, int NW, bool F8>
-__global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? 2 : 1)
+__global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? (F8 ? 3 : 2) : 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeParams p)
 {

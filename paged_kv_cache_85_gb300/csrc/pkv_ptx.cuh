@@ -192,6 +192,53 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w)
     return r;
 }
 
+// Four E4M3 codes (byte i of `w` is code i) -> two f16x2: codes 0,1 in `lo`,
+// codes 2,3 in `hi`, the lower-numbered code in the low half (exact).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// f16x2 -> two fp32 (exact): the low half in .x.
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w)
+{
+    float2 r;
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(w));
+    return r;
+}
+
+// D = A(16x32, row) * B(32x8, col) + D, E4M3 inputs, fp32 accumulators.
+// Lane l holds A rows l/4 (a0, a2) and l/4 + 8 (a1, a3), columns 4(l%4)..+3
+// (a0, a1) and 16 + 4(l%4)..+3 (a2, a3); B rows 4(l%4)..+3 (b0) and
+// 16 + 4(l%4)..+3 (b1) of column l/4; four codes per register, the lowest
+// column (row) in the low byte.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 b16 matrix held one row pair per lane (lane l: row
+// l/4, columns 2(l%4), 2(l%4)+1): afterwards lane l holds row l/4 of the
+// transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // Two fp32 -> two E4M3 codes (nearest even, finite saturation); `lo` in the
 // low byte of the result.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
