@@ -56,6 +56,11 @@ def _load():
             lib.oracle_paged_attn_decode.restype = i64
             lib.oracle_paged_attn_decode.argtypes = [
                 P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32, f32, P]
+            lib.oracle_paged_prefill_pairs.restype = i64
+            lib.oracle_paged_prefill_pairs.argtypes = [
+                P, P, P, P, i32, P, P, i32, i32, i32, i32, i64, i32, f32, P, i64, P]
+            lib.oracle_dense_causal_attn.restype = None
+            lib.oracle_dense_causal_attn.argtypes = [P, P, P, i32, i32, i32, i32, i32, f32, P]
             lib.oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.oracle_e4m3_encode.argtypes = [f32]
             lib.oracle_e4m3_decode.restype = ctypes.c_double
@@ -251,3 +256,58 @@ def paged_attn_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale
     kd = dequant_fp8(k_cache, k_scale)
     vd = dequant_fp8(v_cache, v_scale)
     return paged_attn_decode_values(q, kd, vd, block_tables, context_lens, scale, pairs=pairs)
+
+
+# ---------------------------------------------------------------- prefill
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k, scale,
+                  pairs=None):
+    """fp64 causal prefill attention over the paged cache.
+
+    q is [Tq, Hq, D] (the sequences' new tokens, concatenated); query i of
+    sequence b sits at position k_len_b - q_len_b + i and attends to positions
+    0 .. that one.  Returns [Tq, Hq, D], or [len(pairs), D] for the listed
+    (token row, head) pairs.
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    bt = _c(block_tables, np.int32)
+    cq = _c(cu_seqlens_q, np.int32)
+    ck = _c(cu_seqlens_k, np.int32)
+    Tq, Hq, D = q.shape
+    NB, bs, Hkv, D2 = kc.shape
+    B = cq.shape[0] - 1
+    assert D2 == D and vc.shape == kc.shape and Hq % Hkv == 0 and ck.shape[0] == B + 1
+    if pairs is None:
+        pr = np.stack(np.meshgrid(np.arange(Tq), np.arange(Hq), indexing="ij"), -1)
+        pr = np.ascontiguousarray(pr.reshape(-1, 2).astype(np.int32))
+    else:
+        pr = _c(pairs, np.int32).reshape(-1, 2)
+    out = np.zeros((pr.shape[0], D), dtype=np.float64)
+    bad = lib.oracle_paged_prefill_pairs(
+        _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cq), _ptr(ck), B, Hq, Hkv, D,
+        NB, bs, float(scale), _ptr(pr), pr.shape[0], _ptr(out))
+    if bad < 0:
+        raise MemoryError("oracle allocation failed")
+    return out.reshape(Tq, Hq, D) if pairs is None else out
+
+
+def dense_causal_attn(q, k, v, scale):
+    """fp64 causal attention of one sequence over contiguous K/V.
+
+    q [Lq, Hq, D], k/v [Lk, Hkv, D] bf16 bits; query i at position Lk - Lq + i.
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    Lq, Hq, D = q.shape
+    Lk, Hkv, D2 = k.shape
+    assert D2 == D and v.shape == k.shape and Lq <= Lk
+    out = np.zeros((Lq, Hq, D), dtype=np.float64)
+    lib.oracle_dense_causal_attn(_ptr(q), _ptr(k), _ptr(v), Lq, Lk, Hq, Hkv, D, float(scale),
+                                 _ptr(out))
+    return out

@@ -389,3 +389,113 @@ int64_t oracle_paged_attn_decode_pairs_f64kv(const uint16_t *q, const double *k_
     free(s);
     return bad;
 }
+
+/*
+ * Paged prefill (MinivLLM guide §4.5, prepare_prefill: the new tokens of all
+ * sequences are flattened into one list whose boundaries cu_seqlens_q marks,
+ * cu_seqlens_k marks each sequence's keys, slot_mapping writes only the
+ * uncached tokens, and block_tables say where KV is read; "Nano-vLLM 源码学习
+ * (2)" §2: the prefix-hit prefill path reads paged KV through block_table).
+ * The pages give no mask; the plain reading for a causal language model:
+ * sequence b has q_len = cu_q[b+1] - cu_q[b] new tokens and a context of
+ * k_len = cu_k[b+1] - cu_k[b] tokens (cached prefix + the new tokens, all
+ * already stored in the cache, q_len <= k_len); its query i sits at position
+ * k_len - q_len + i and attends to the tokens at positions 0 .. that position.
+ * Each (query row, head) is thus decode attention over its first position + 1
+ * tokens, computed here by the same definition as decode_one.
+ *
+ * pairs: (token row r in [0, cu_q[B]), query head h); out is [n_pairs, D].
+ * Returns the number of pairs left at zero because their lengths are
+ * inconsistent or a needed block-table entry is outside [0, NB).
+ */
+int64_t oracle_paged_prefill_pairs(const uint16_t *q, const uint16_t *k_cache,
+                                   const uint16_t *v_cache, const int32_t *block_tables,
+                                   int MBS, const int32_t *cu_q, const int32_t *cu_k, int B,
+                                   int Hq, int Hkv, int D, int64_t NB, int bs, float scale,
+                                   const int32_t *pairs, int64_t n_pairs, double *out)
+{
+    int G = Hq / Hkv;
+    int64_t bad = 0;
+    int max_n = MBS * bs;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_n > 0 ? max_n : 1));
+    if (!s)
+        return -1;
+    for (int64_t i = 0; i < n_pairs; i++) {
+        int r = pairs[2 * i], h = pairs[2 * i + 1];
+        double *o = out + i * D;
+        for (int d = 0; d < D; d++)
+            o[d] = 0.0;
+        int b = 0;
+        while (b < B && cu_q[b + 1] <= r)
+            b++;
+        if (b == B || r < cu_q[b]) {
+            bad++;
+            continue;
+        }
+        int q_len = cu_q[b + 1] - cu_q[b];
+        int k_len = cu_k[b + 1] - cu_k[b];
+        if (k_len < q_len || k_len > max_n) {
+            bad++;
+            continue;
+        }
+        int n = k_len - q_len + (r - cu_q[b]) + 1;
+        const uint16_t *qr = q + ((int64_t)r * Hq + h) * D;
+        const int32_t *table = block_tables + (int64_t)b * MBS;
+        if (decode_one(qr, k_cache, v_cache, table, n, Hkv, h / G, D, NB, bs, (double)scale,
+                       o, s) != 0) {
+            for (int d = 0; d < D; d++)
+                o[d] = 0.0;
+            bad++;
+        }
+    }
+    free(s);
+    return bad;
+}
+
+/*
+ * Dense causal attention of one sequence over contiguous K/V, written apart
+ * from the paged routines (explicit score row with -inf above the diagonal)
+ * so that the paged prefill can be checked against it: the paged cache must
+ * give the result of attending over the contiguous context.
+ * q [Lq, Hq, D], k/v [Lk, Hkv, D] (Lq <= Lk; query i is at position
+ * Lk - Lq + i); out [Lq, Hq, D] fp64.
+ */
+void oracle_dense_causal_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int Lq,
+                              int Lk, int Hq, int Hkv, int D, float scale, double *out)
+{
+    int G = Hq / Hkv;
+    double *row = (double *)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
+    for (int i = 0; i < Lq; i++) {
+        int last = Lk - Lq + i; /* highest key position this query may see */
+        for (int h = 0; h < Hq; h++) {
+            int kvh = h / G;
+            double *o = out + ((int64_t)i * Hq + h) * D;
+            double m = -INFINITY;
+            for (int j = 0; j < Lk; j++) {
+                if (j > last) {
+                    row[j] = -INFINITY;
+                    continue;
+                }
+                double dot = 0.0;
+                for (int d = 0; d < D; d++)
+                    dot += bf16_to_f64(q[((int64_t)i * Hq + h) * D + d]) *
+                           bf16_to_f64(k[((int64_t)j * Hkv + kvh) * D + d]);
+                row[j] = (double)scale * dot;
+                if (row[j] > m)
+                    m = row[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j < Lk; j++) {
+                row[j] = exp(row[j] - m); /* exp(-inf) = 0 for masked keys */
+                l += row[j];
+            }
+            for (int d = 0; d < D; d++) {
+                double acc = 0.0;
+                for (int j = 0; j < Lk; j++)
+                    acc += row[j] * bf16_to_f64(v[((int64_t)j * Hkv + kvh) * D + d]);
+                o[d] = acc / l;
+            }
+        }
+    }
+    free(row);
+}

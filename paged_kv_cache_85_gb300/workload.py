@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for paged decode attention.
+"""Seeded synthetic inputs for paged decode and prefill attention.
 
 This module only *draws* inputs: context lengths, block placement, block
 tables, slot mappings and bf16 tensors.  It holds none of the arithmetic of
@@ -257,3 +257,197 @@ def config_workload(idx: int, seed: int = 0, poison_unused: bool = False) -> Wor
             recipe="8 seqs x 32768, bs256, 32Q/8KV, D128, first 8192 tokens' blocks shared",
         )
     raise ValueError(f"no config {idx}")
+
+
+# ---------------------------------------------------------------- prefill
+
+
+@dataclasses.dataclass
+class PrefillWorkload:
+    """One prefill step's inputs: the new tokens of B sequences, flattened.
+
+    Sequence b has ``q_lens[b]`` new tokens after a cached prefix of
+    ``k_lens[b] - q_lens[b]`` tokens (whole blocks, as prefix caching keeps
+    them).  The step stores the new tokens' K/V through ``slot_mapping``
+    (only uncached tokens get slots) and then attends through
+    ``block_tables`` (MinivLLM guide, §4.5 ``prepare_prefill``).
+    """
+
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    bs: int
+    NB: int
+    MBS: int
+    scale: float
+    q_lens: np.ndarray  # int32 [B]
+    k_lens: np.ndarray  # int32 [B]; cached prefix + new tokens
+    cu_seqlens_q: np.ndarray  # int32 [B + 1]
+    cu_seqlens_k: np.ndarray  # int32 [B + 1]
+    block_tables: np.ndarray  # int32 [B, MBS]; -1 past the used blocks
+    q: np.ndarray  # u16 bf16 [Tq, Hq, D]
+    k_cache: np.ndarray  # u16 bf16 [NB, bs, Hkv, D]
+    v_cache: np.ndarray  # u16 bf16 [NB, bs, Hkv, D]
+    k_new: np.ndarray  # u16 bf16 [Tq, Hkv, D]
+    v_new: np.ndarray  # u16 bf16 [Tq, Hkv, D]
+    slot_mapping: np.ndarray  # int64 [Tq]
+    recipe: str = ""
+
+    @property
+    def Tq(self) -> int:
+        return int(self.cu_seqlens_q[-1])
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def max_seqlen_q(self) -> int:
+        return int(self.q_lens.max())
+
+    def attended_keys(self) -> int:
+        """Sum over query tokens of the keys each one sees (causal)."""
+        tot = 0
+        for ql, kl in zip(self.q_lens.tolist(), self.k_lens.tolist()):
+            # query i sees kl - ql + i + 1 keys
+            tot += ql * (kl - ql) + ql * (ql + 1) // 2
+        return tot
+
+    def flops(self) -> int:
+        """Algorithmic FLOPs: 2 per multiply-add of q.K and of P.V, causal keys only."""
+        return 4 * self.attended_keys() * self.Hq * self.D
+
+    def kv_bytes(self) -> int:
+        """K and V bytes of every sequence's context, read once."""
+        return int(self.k_lens.astype(np.int64).sum()) * self.Hkv * self.D * 2 * 2
+
+    def io_bytes(self) -> int:
+        """K/V once + q + out + tables + cu_seqlens."""
+        tables = sum((int(n) + self.bs - 1) // self.bs for n in self.k_lens) * 4
+        return self.kv_bytes() + 2 * self.Tq * self.Hq * self.D * 2 + tables + 8 * (self.B + 1)
+
+
+def cu_seqlens(lengths) -> np.ndarray:
+    """[0, l0, l0 + l1, ...] as int32: the boundaries of flattened sequences."""
+    out = np.zeros(len(lengths) + 1, dtype=np.int32)
+    out[1:] = np.cumsum(np.asarray(lengths, dtype=np.int64))
+    return out
+
+
+def make_prefill_workload(
+    name: str,
+    Hq: int,
+    Hkv: int,
+    D: int,
+    bs: int,
+    q_lens,
+    cached_lens,
+    NB: int | None = None,
+    shared_prefix_tokens: int = 0,
+    poison_unused: bool = False,
+    recipe: str = "",
+    rng: np.random.Generator | None = None,
+    seed: int = 0,
+) -> PrefillWorkload:
+    """Draw one prefill step's inputs.
+
+    Draw order: block permutation -> q -> k_cache -> v_cache -> new k -> new v.
+    Cached prefixes are whole blocks.  With ``shared_prefix_tokens`` the first
+    blocks of every table are the same physical ids (a prefix-cache hit shared
+    by all sequences); the rest of each table is the sequence's own blocks,
+    taken from a seeded permutation of ``[0, NB)``.
+    """
+    if rng is None:
+        rng = np.random.default_rng(seed)
+    ql = np.asarray(q_lens, dtype=np.int32)
+    cl = np.asarray(cached_lens, dtype=np.int32)
+    B = int(ql.shape[0])
+    assert cl.shape == ql.shape and (ql >= 1).all() and (cl >= 0).all()
+    assert (cl % bs == 0).all(), "prefix caching keeps whole blocks"
+    assert shared_prefix_tokens % bs == 0 and (cl >= shared_prefix_tokens).all()
+    kl = cl + ql
+    nblk = (kl.astype(np.int64) + bs - 1) // bs
+    MBS = int(nblk.max())
+    n_shared = shared_prefix_tokens // bs
+    own = nblk - n_shared
+    need = n_shared + int(own.sum())
+    if NB is None:
+        NB = int(math.ceil(1.25 * need))
+    assert NB >= need
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = np.full((B, MBS), -1, dtype=np.int32)
+    cur = n_shared
+    for b in range(B):
+        tables[b, :n_shared] = perm[:n_shared]
+        k = int(own[b])
+        tables[b, n_shared : n_shared + k] = perm[cur : cur + k]
+        cur += k
+    cq = cu_seqlens(ql)
+    Tq = int(cq[-1])
+    q = _randn_bf16(rng, (Tq, Hq, D))
+    k_cache = _randn_bf16(rng, (NB, bs, Hkv, D))
+    v_cache = _randn_bf16(rng, (NB, bs, Hkv, D))
+    k_new = _randn_bf16(rng, (Tq, Hkv, D))
+    v_new = _randn_bf16(rng, (Tq, Hkv, D))
+    slots = np.empty(Tq, dtype=np.int64)
+    for b in range(B):
+        pos = np.arange(int(cl[b]), int(kl[b]), dtype=np.int64)
+        slots[cq[b] : cq[b + 1]] = tables[b, pos // bs].astype(np.int64) * bs + pos % bs
+    if poison_unused:
+        poison_unused_slots(k_cache, v_cache, tables, kl, bs)
+    return PrefillWorkload(
+        name=name, B=B, Hq=Hq, Hkv=Hkv, D=D, bs=bs, NB=NB, MBS=MBS,
+        scale=float(np.float32(1.0 / math.sqrt(D))), q_lens=ql, k_lens=kl.astype(np.int32),
+        cu_seqlens_q=cq, cu_seqlens_k=cu_seqlens(kl), block_tables=tables, q=q,
+        k_cache=k_cache, v_cache=v_cache, k_new=k_new, v_new=v_new, slot_mapping=slots,
+        recipe=recipe,
+    )
+
+
+# Prefill steps shaped like the pages' settings: a token budget of
+# max_num_batched_tokens = 16384 per step and max_model_len = 4096
+# ("Nano-vLLM 源码学习(2)", §2 Config), block sizes 256 (nano-vllm) and 16
+# (vLLM 0.7.3), cached prefixes from prefix caching.  Index 0 is tiny.
+PREFILL_CONFIG_NAMES = [
+    "tiny_paged_prefill",
+    "qwen3_prefill_16k",
+    "vllm_bs16_prefill_ragged",
+    "shared_prefix_prefill",
+]
+
+
+def prefill_config_workload(idx: int, seed: int = 0, poison_unused: bool = False) -> PrefillWorkload:
+    """The prefill steps (seeded with ``SeedSequence([seed, 100 + idx])``)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 100 + idx]))
+    name = PREFILL_CONFIG_NAMES[idx]
+    if idx == 0:
+        return make_prefill_workload(
+            name, Hq=4, Hkv=2, D=64, bs=16, q_lens=[1, 5, 17, 40], cached_lens=[0, 16, 32, 0],
+            NB=64, rng=rng, poison_unused=poison_unused,
+            recipe="4 seqs, new {1,5,17,40} after cached {0,16,32,0}, bs16, 4Q/2KV, D64, NB=64",
+        )
+    if idx == 1:
+        return make_prefill_workload(
+            name, Hq=16, Hkv=8, D=128, bs=256, q_lens=[2048] * 8,
+            cached_lens=[0, 0, 0, 0, 256, 512, 1024, 2048], rng=rng, poison_unused=poison_unused,
+            recipe="8 seqs x 2048 new tokens (16384), cached {0,0,0,0,256,512,1024,2048}, "
+                   "bs256, 16Q/8KV, D128",
+        )
+    if idx == 2:
+        ql = rng.integers(1, 1023, size=32, endpoint=True)
+        cl = 16 * rng.integers(0, 64, size=32, endpoint=True)
+        return make_prefill_workload(
+            name, Hq=32, Hkv=8, D=128, bs=16, q_lens=ql, cached_lens=cl, rng=rng,
+            poison_unused=poison_unused,
+            recipe="32 seqs, new U[1,1023], cached 16*U[0,64], bs16, 32Q/8KV, D128",
+        )
+    if idx == 3:
+        return make_prefill_workload(
+            name, Hq=16, Hkv=8, D=128, bs=256, q_lens=[1024] * 16, cached_lens=[2048] * 16,
+            shared_prefix_tokens=2048, rng=rng, poison_unused=poison_unused,
+            recipe="16 seqs x 1024 new tokens after one shared cached 2048-token prefix, "
+                   "bs256, 16Q/8KV, D128",
+        )
+    raise ValueError(f"no prefill config {idx}")
