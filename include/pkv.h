@@ -155,6 +155,46 @@ pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void 
                                  void *stream);
 
 /*
+ * pkv_paged_prefill - causal attention of a prefill step's new tokens over
+ * their sequences' paged contexts.
+ *
+ * MinivLLM guide "HowToApproachvLLM", section 4.5 (prepare_prefill): the
+ * new tokens of all B sequences are flattened into one list, cu_seqlens_q
+ * and cu_seqlens_k mark the sequences' boundaries, slot_mapping writes the
+ * uncached tokens' K/V (pkv_store_kvcache, called first) and block_tables
+ * say where KV is read; "Nano-vLLM 源码学习(2)" section 2: the prefix-hit
+ * prefill path reads paged KV through block_table.  The pages give no mask;
+ * the plain causal reading is used: sequence b has q_len = cu_seqlens_q[b+1]
+ * - cu_seqlens_q[b] new tokens and k_len = cu_seqlens_k[b+1] -
+ * cu_seqlens_k[b] context tokens (cached prefix + the new tokens); new token
+ * i sits at position k_len - q_len + i and attends to positions 0 .. that
+ * one, read through block_tables[b]:
+ *   out[cu_seqlens_q[b] + i, h, :] = softmax(scale * q . K^T) . V
+ * with query head h reading KV head h / (Hq / Hkv).
+ *
+ *   q             device, bf16 [Tq, Hq, D] contiguous, 16-byte aligned
+ *   k_cache/v_cache device, bf16 [NB, bs, Hkv, D] (as pkv_store_kvcache)
+ *   block_tables  device, int32 [B, MBS]; entries past ceil(k_len / bs) unread
+ *   cu_seqlens_q  device, int32 [B + 1], non-decreasing, cu_seqlens_q[B] <= Tq
+ *   cu_seqlens_k  device, int32 [B + 1]; q_len <= k_len <= MBS * bs
+ *   max_seqlen_q  host bound on every q_len (sizes the grid)
+ *   out           device, bf16 [Tq, Hq, D]; rows not covered by cu_seqlens_q
+ *                 are left untouched
+ * D in {64, 128}; Hq / Hkv in {1, 2, 4, 8}; bs a multiple of 16.  No
+ * workspace.  Device-side problems set err_flag bits and never trap: a
+ * sequence whose lengths are inconsistent (or q_len > max_seqlen_q) is
+ * skipped with PKV_FLAG_BAD_CONTEXT_LEN; a table entry outside [0, NB) sets
+ * PKV_FLAG_BAD_BLOCK and its 16-token boxes are left out of the softmax.
+ * Host-side errors return a status before any launch; B, Tq or
+ * max_seqlen_q == 0 is a no-op.
+ */
+pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, int MBS, const int32_t *cu_seqlens_q,
+                             const int32_t *cu_seqlens_k, int B, int64_t Tq, int max_seqlen_q,
+                             int Hq, int Hkv, int D, int64_t NB, int bs, float scale, void *out,
+                             int32_t *err_flag, void *stream);
+
+/*
  * FP8 KV cache ("VLLM-0.7.3 源码" section 5.3: kv_cache_dtype can store the
  * KV cache in FP8 while the output side keeps higher-precision compute).
  * The page gives no scale convention; these calls take the plain one: a

@@ -28,6 +28,7 @@ __all__ = [
     "store_kvcache",
     "paged_attn_decode",
     "store_kvcache_fp8",
+    "paged_prefill",
     "paged_attn_decode_fp8",
     "decode_workspace_bytes",
     "load_library",
@@ -90,6 +91,9 @@ def load_library():
         lib.pkv_paged_attn_decode_fp8.restype = i32
         lib.pkv_paged_attn_decode_fp8.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32,
                                                   f32, f32, f32, P, P, sz, i32, P, P]
+        lib.pkv_paged_prefill.restype = i32
+        lib.pkv_paged_prefill.argtypes = [P, P, P, P, i32, P, P, i32, i64, i32, i32, i32, i32,
+                                          i64, i32, f32, P, P, P]
         lib.pkv_last_error.restype = ctypes.c_char_p
         lib.pkv_last_error.argtypes = []
         lib.pkv_version.restype = i32
@@ -290,4 +294,43 @@ def paged_attn_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale
             max(MBS, 1), context_lens.data_ptr(), B, Hq, Hkv, D, NB, bs, float(scale),
             float(k_scale), float(v_scale), out.data_ptr(), ws_ptr, ws_bytes, int(max_ctas),
             err_flag.data_ptr() if err_flag is not None else None, stream))
+    return out
+
+
+# ---------------------------------------------------------------- prefill
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                  scale, out, err_flag=None):
+    """Causal attention of a prefill step's new tokens over their paged contexts.
+
+    q / out are [Tq, Hq, D] bf16 (the sequences' new tokens, concatenated);
+    cu_seqlens_q / cu_seqlens_k are int32 [B + 1] on the device; new token i
+    of sequence b attends to context positions 0 .. k_len_b - q_len_b + i.
+    Store the new tokens' K/V first (``store_kvcache``).  Returns ``out``.
+    """
+    import torch
+
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k_cache, "k_cache", torch.bfloat16, 4)
+    _require(v_cache, "v_cache", torch.bfloat16, 4)
+    _require(block_tables, "block_tables", torch.int32, 2)
+    _require(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _require(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    _require(out, "out", torch.bfloat16, 3)
+    Tq, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape:
+        raise ValueError("paged_prefill: shapes do not match")
+    B = cu_seqlens_q.shape[0] - 1
+    if B < 0 or cu_seqlens_k.shape[0] != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("paged_prefill: cu_seqlens / block_tables batch sizes differ")
+    lib = _lib or load_library()
+    idx = q.get_device()
+    with _on_device(idx):
+        _check(lib.pkv_paged_prefill(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+            max(block_tables.shape[1], 1), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, Tq,
+            int(max_seqlen_q), Hq, Hkv, D, NB, bs, float(scale), out.data_ptr(),
+            err_flag.data_ptr() if err_flag is not None else None, _raw_stream(idx)))
     return out

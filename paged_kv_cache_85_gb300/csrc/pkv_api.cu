@@ -14,6 +14,7 @@
 #include "pkv.h"
 #include "pkv_decode.cuh"
 #include "pkv_kernels.h"
+#include "pkv_prefill.cuh"
 
 namespace pkv {
 #define PKV_DECLARE_SHAPE(D, NW)                                                                  \
@@ -36,6 +37,26 @@ PKV_DECLARE_SHAPE8(64, 8)
 PKV_DECLARE_SHAPE8(128, 4)
 PKV_DECLARE_SHAPE8(128, 8)
 #undef PKV_DECLARE_SHAPE8
+cudaError_t launch_prefill_d64(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                               const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_prefill_d128(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                                const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream);
+const void *prefill_kernel_d64(int G);
+const void *prefill_kernel_d128(int G);
+
+cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                           const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream)
+{
+    return D == 128 ? launch_prefill_d128(G, tmk, tmv, p, grid, smem, stream)
+                    : launch_prefill_d64(G, tmk, tmv, p, grid, smem, stream);
+}
+
+const void *prefill_kernel(int D, int G)
+{
+    return D == 128 ? prefill_kernel_d128(G) : prefill_kernel_d64(G);
+}
+
+size_t prefill_smem_bytes(int D) { return prefill_smem_layout(D).total; }
 
 const void *decode_kernel(int D, int NW, int G, bool f8)
 {
@@ -96,6 +117,7 @@ struct DeviceState {
     int dev = 0;
     int sms = 0;
     bool smem_set[2][2][2][9] = {};  // [fp8][D == 128][NW == 8][G]
+    bool pf_smem_set[2][9] = {};     // prefill: [D == 128][G]
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -513,6 +535,90 @@ pkv_status pkv_paged_attn_decode_fp8(const void *q, const void *k_cache, const v
     return decode_impl(q, k_cache, v_cache, block_tables, MBS, context_lens, B, Hq, Hkv, D, NB, bs,
                        scale, out, workspace, workspace_bytes, max_ctas, err_flag, stream, true,
                        k_scale, v_scale);
+}
+
+pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, int MBS, const int32_t *cu_seqlens_q,
+                             const int32_t *cu_seqlens_k, int B, int64_t Tq, int max_seqlen_q,
+                             int Hq, int Hkv, int D, int64_t NB, int bs, float scale, void *out,
+                             int32_t *err_flag, void *stream)
+{
+    if (B < 0 || Tq < 0 || max_seqlen_q < 0 || NB < 1 || MBS < 1 || bs < 1 || Hq < 1 || Hkv < 1)
+        return fail(PKV_ERR_INVALID_ARG, "paged_prefill: bad sizes B=%d Tq=%lld max_seqlen_q=%d "
+                    "NB=%lld MBS=%d bs=%d Hq=%d Hkv=%d", B, (long long)Tq, max_seqlen_q,
+                    (long long)NB, MBS, bs, Hq, Hkv);
+    if (Hq % Hkv != 0)
+        return fail(PKV_ERR_INVALID_ARG, "paged_prefill: Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
+    const int G = Hq / Hkv;
+    if (!group_supported(G))
+        return fail(PKV_ERR_UNSUPPORTED, "paged_prefill: Hq/Hkv=%d not in {1,2,4,8}", G);
+    if (D != 64 && D != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_prefill: head_dim %d not in {64,128}", D);
+    if (bs % pkv::kBox != 0)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_prefill: block_size %d not a multiple of 16", bs);
+    if (!std::isfinite(scale))
+        return fail(PKV_ERR_INVALID_ARG, "paged_prefill: scale is not finite");
+    if ((long long)NB * bs >= 0x7fffffffLL || (long long)MBS * bs >= 0x7fffffffLL)
+        return fail(PKV_ERR_INVALID_ARG, "paged_prefill: NB*bs and MBS*bs must be < 2^31");
+    if (Tq >= 0x7fffffffLL || B > 65535)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_prefill: Tq must be < 2^31 and B <= 65535");
+    if (B == 0 || Tq == 0 || max_seqlen_q == 0)
+        return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !cu_seqlens_q || !cu_seqlens_k || !out)
+        return fail(PKV_ERR_INVALID_ARG, "paged_prefill: null pointer");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+        return fail(PKV_ERR_INVALID_ARG, "paged_prefill: misaligned pointer");
+    const long long tiles = ((long long)max_seqlen_q * G + pkv::kPrefillRows - 1) / pkv::kPrefillRows;
+    if (tiles > 0x7fffffffLL)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_prefill: max_seqlen_q too large");
+
+    DeviceState *st = nullptr;
+    pkv_status ps = device_state(&st);
+    if (ps != PKV_OK)
+        return ps;
+    const void *kfn = pkv::prefill_kernel(D, G);
+    const size_t smem = pkv::prefill_smem_bytes(D);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        bool &set = st->pf_smem_set[D == 128][G];
+        if (!set) {
+            cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess)
+                return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            set = true;
+        }
+    }
+    CUtensorMap tmk, tmv;
+    const long long tokens = (long long)NB * bs;
+    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D)) != PKV_OK)
+        return ps;
+    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D)) != PKV_OK)
+        return ps;
+    pkv::PrefillParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.out = static_cast<uint16_t *>(out);
+    p.block_tables = block_tables;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.err_flag = err_flag;
+    p.Tq = Tq;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.MBS = MBS;
+    p.bs = bs;
+    p.NB = (int)NB;
+    p.max_q = max_seqlen_q;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaError_t e = pkv::launch_prefill(D, G, &tmk, &tmv, p, dim3((unsigned)tiles, Hkv, B), smem,
+                                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "paged_prefill launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
 }
 
 pkv_status pkv_store_kvcache_fp8(const void *k, const void *v, void *k_cache, void *v_cache,

@@ -48,7 +48,6 @@
 namespace pkv {
 
 constexpr int kLookahead = 4;  // boxes per worker whose block ids are loaded ahead of use
-constexpr int kHalfBytes = kBox * 128;  // one 64-column half of a box: 16 rows of 128 B
 
 // Per-worker box descriptor of a stage, written by the producer.
 struct __align__(16) BoxMeta {
@@ -68,7 +67,6 @@ struct DecodeSmem {
     size_t kv, q, full, empty, meta, pb, len, scan, total;
 };
 
-__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int NW, int stages, int B,
                                                          int kv_elem_bytes = 2)

@@ -1,0 +1,14 @@
+// Instantiations of the paged prefill kernel, head_dim 128, G = 1, 2, 4, 8.
+#include "pkv_prefill.cuh"
+
+namespace pkv {
+
+cudaError_t launch_prefill_d128(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                               const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream)
+{
+    return launch_prefill_d<128>(G, tmk, tmv, p, grid, smem, stream);
+}
+
+const void *prefill_kernel_d128(int G) { return prefill_kernel_d<128>(G); }
+
+} // namespace pkv

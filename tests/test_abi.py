@@ -116,3 +116,23 @@ def test_fp8_argument_errors_need_no_gpu(cuda_lib_path):
                 None, None, 0, 0, None, None) == 1
     assert dec8(None, None, None, None, 1, None, 0, 4, 4, 64, 1, 16, 1.0, 1.0, 1.0,
                 None, None, 0, 0, None, None) == 0
+
+
+def test_prefill_argument_errors_need_no_gpu(cuda_lib_path):
+    lib = ctypes.CDLL(cuda_lib_path)
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    lib.pkv_last_error.restype = ctypes.c_char_p
+    f = lib.pkv_paged_prefill
+    f.restype = i32
+    f.argtypes = [P, P, P, P, i32, P, P, i32, i64, i32, i32, i32, i32, i64, i32, f32, P, P, P]
+    # (q, kc, vc, tables, MBS, cu_q, cu_k, B, Tq, max_q, Hq, Hkv, D, NB, bs, scale, out, err, stream)
+    assert f(None, None, None, None, 4, None, None, 2, 10, 5, 6, 4, 64, 8, 16, 1.0, None, None, None) == 1
+    assert b"multiple" in lib.pkv_last_error()
+    assert f(None, None, None, None, 4, None, None, 2, 10, 5, 4, 4, 96, 8, 16, 1.0, None, None, None) == 2
+    assert f(None, None, None, None, 4, None, None, 2, 10, 5, 4, 4, 64, 8, 8, 1.0, None, None, None) == 2
+    assert f(None, None, None, None, 4, None, None, 2, 10, 5, 12, 4, 64, 8, 16, 1.0, None, None, None) == 2
+    assert f(None, None, None, None, 4, None, None, 2, 10, 5, 4, 4, 64, 8, 16, float("inf"), None, None, None) == 1
+    assert f(None, None, None, None, 4, None, None, -1, 10, 5, 4, 4, 64, 8, 16, 1.0, None, None, None) == 1
+    # nothing to do: no launch, no device needed
+    assert f(None, None, None, None, 4, None, None, 0, 0, 0, 4, 4, 64, 8, 16, 1.0, None, None, None) == 0
+    assert f(None, None, None, None, 4, None, None, 2, 10, 5, 4, 4, 64, 8, 16, 1.0, None, None, None) == 1  # null

@@ -1,0 +1,264 @@
+"""GPU parity of the paged prefill against the CPU oracle, through the C ABI.
+
+The step is store_kvcache (bit-exact over the whole cache) then
+paged_prefill.  Attention must match the fp64 oracle to max-abs <= 1e-2 and
+mean-abs <= 1e-3 (bf16 in and out), over every output of the small cases and
+over sampled (token row, head) pairs of the 16k-token steps; every output of
+the large steps must be finite.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_85_gb300 import workload as wl
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 1e-2
+MEAN_ABS = 1e-3
+
+
+@pytest.fixture(scope="module")
+def pkv(cuda_lib_path):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_85_gb300 as m
+
+    m.load_library()
+    return m
+
+
+def bf16_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def bits_host(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def to_dev(w):
+    return dict(
+        q=bf16_dev(w.q), k_cache=bf16_dev(w.k_cache), v_cache=bf16_dev(w.v_cache),
+        k_new=bf16_dev(w.k_new), v_new=bf16_dev(w.v_new),
+        slots=torch.from_numpy(w.slot_mapping).cuda(),
+        tables=torch.from_numpy(w.block_tables).cuda(),
+        cu_q=torch.from_numpy(w.cu_seqlens_q).cuda(), cu_k=torch.from_numpy(w.cu_seqlens_k).cuda(),
+    )
+
+
+def run_step(pkv, w, d, err=None, out=None, store=True):
+    if store:
+        pkv.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slots"],
+                          err_flag=err)
+    if out is None:
+        out = torch.empty_like(d["q"])
+    pkv.paged_prefill(d["q"], d["k_cache"], d["v_cache"], d["tables"], d["cu_q"], d["cu_k"],
+                      w.max_seqlen_q, w.scale, out, err_flag=err)
+    torch.cuda.synchronize()
+    return out
+
+
+def stored(w):
+    kc, vc, bad = oracle.store_kvcache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    assert bad == 0
+    return kc, vc
+
+
+def compare(got, ref, what=""):
+    got = wl.bf16_bits_to_f32(got).astype(np.float64)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_ABS, f"{what}: max-abs {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}"
+    assert err.mean() <= MEAN_ABS, f"{what}: mean-abs {err.mean():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def sample_pairs(w, rng, per_seq=48):
+    """(row, head) pairs: every sequence's first and last tokens, tokens on
+    both sides of the kernel's 112-row tile boundaries, and random tokens;
+    random heads."""
+    tpc = 112 // w.G
+    rows = []
+    for b in range(w.B):
+        ql = int(w.q_lens[b])
+        toks = {0, ql - 1, ql // 2}
+        for k in range(1, ql // tpc + 1):
+            toks.update({k * tpc - 1, min(k * tpc, ql - 1)})
+        toks.update(rng.integers(0, ql, size=per_seq).tolist())
+        rows.extend(int(w.cu_seqlens_q[b]) + t for t in sorted(toks) if 0 <= t < ql)
+    heads = rng.integers(0, w.Hq, size=len(rows))
+    pairs = np.stack([np.array(rows), heads], 1).astype(np.int32)
+    # a few rows with every head
+    for r in rng.choice(len(rows), size=min(8, len(rows)), replace=False):
+        pairs = np.concatenate([pairs, np.stack([np.full(w.Hq, rows[r]), np.arange(w.Hq)], 1)
+                                .astype(np.int32)])
+    return pairs
+
+
+_cache = {}
+
+
+def config(idx):
+    if idx not in _cache:
+        _cache.clear()
+        w = wl.prefill_config_workload(idx)
+        kc, vc = stored(w)
+        if idx == 0:
+            ref, pairs = oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q,
+                                              w.cu_seqlens_k, w.scale), None
+        else:
+            pairs = sample_pairs(w, np.random.default_rng(idx))
+            ref = oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q,
+                                       w.cu_seqlens_k, w.scale, pairs=pairs)
+        _cache[idx] = (w, kc, vc, ref, pairs)
+    return _cache[idx]
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3])
+def test_config_store_bitexact_and_prefill_parity(pkv, idx):
+    w, kc, vc, ref, pairs = config(idx)
+    d = to_dev(w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_step(pkv, w, d, err=err)
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(bits_host(d["k_cache"]), kc)
+    np.testing.assert_array_equal(bits_host(d["v_cache"]), vc)
+    o = bits_host(out)
+    assert np.isfinite(wl.bf16_bits_to_f32(o)).all()
+    if pairs is None:
+        compare(o, ref, w.name)
+    else:
+        compare(o[pairs[:, 0], pairs[:, 1]], ref, w.name)
+
+
+def _random(rng, G, D, bs, q_lens, cached, NB=None, Hkv=2, poison=False):
+    return wl.make_prefill_workload("rand", Hq=G * Hkv, Hkv=Hkv, D=D, bs=bs, q_lens=q_lens,
+                                    cached_lens=cached, NB=NB, rng=rng, poison_unused=poison)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("bs", [16, 32, 256])
+def test_group_dim_block_variants(pkv, G, D, bs):
+    rng = np.random.default_rng(500 + 7 * G + D + bs)
+    q_lens = [1, 15, 16, 17, 63, 64, 65, 130, 200][: 4 + G // 2]
+    cached = [bs * int(c) for c in rng.integers(0, 3, size=len(q_lens))]
+    w = _random(rng, G, D, bs, q_lens, cached)
+    kc, vc = stored(w)
+    ref = oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k,
+                               w.scale)
+    compare(bits_host(run_step(pkv, w, to_dev(w))), ref, f"G={G} D={D} bs={bs}")
+
+
+def test_long_context_rows_across_many_tiles(pkv):
+    """One long sequence (cached 1024 + 700 new) at G = 2: many K tiles and query tiles."""
+    rng = np.random.default_rng(510)
+    w = _random(rng, 2, 128, 256, [700, 3], [1024, 256])
+    kc, vc = stored(w)
+    ref = oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k,
+                               w.scale)
+    compare(bits_host(run_step(pkv, w, to_dev(w))), ref, "long")
+
+
+def test_first_token_of_a_fresh_sequence_returns_its_v_bitexact(pkv):
+    rng = np.random.default_rng(511)
+    w = _random(rng, 4, 128, 16, [5, 40, 1], [0, 0, 0])
+    kc, vc = stored(w)
+    out = bits_host(run_step(pkv, w, to_dev(w)))
+    for b in range(w.B):
+        r = int(w.cu_seqlens_q[b])
+        blk = w.block_tables[b, 0]
+        for h in range(w.Hq):
+            np.testing.assert_array_equal(out[r, h], vc[blk, 0, h // w.G])
+
+
+def test_nan_in_unread_slots_changes_nothing(pkv):
+    rng = np.random.default_rng(512)
+    q_lens, cached = [3, 17, 40, 1], [16, 0, 32, 48]
+    w = _random(rng, 4, 128, 16, q_lens, cached)
+    clean = bits_host(run_step(pkv, w, to_dev(w)))
+    kc, vc = stored(w)
+    wl.poison_unused_slots(kc, vc, w.block_tables, w.k_lens, w.bs)
+    d = to_dev(w)
+    d["k_cache"], d["v_cache"] = bf16_dev(kc), bf16_dev(vc)
+    out = bits_host(run_step(pkv, w, d, store=False))
+    assert np.isfinite(wl.bf16_bits_to_f32(out)).all()
+    np.testing.assert_array_equal(out, clean)
+
+
+def test_block_permutation_gives_identical_output(pkv):
+    rng = np.random.default_rng(513)
+    w = _random(rng, 2, 128, 16, [20, 77, 5], [32, 0, 64], NB=64)
+    kc, vc = stored(w)
+    d = to_dev(w)
+    d["k_cache"], d["v_cache"] = bf16_dev(kc), bf16_dev(vc)
+    a = bits_host(run_step(pkv, w, d, store=False))
+    pi = rng.permutation(w.NB)
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[pi], vc2[pi] = kc, vc
+    d["k_cache"], d["v_cache"] = bf16_dev(kc2), bf16_dev(vc2)
+    d["tables"] = torch.from_numpy(
+        np.where(w.block_tables >= 0, pi[np.maximum(w.block_tables, 0)], -1).astype(np.int32)).cuda()
+    b = bits_host(run_step(pkv, w, d, store=False))
+    np.testing.assert_array_equal(a, b)
+
+
+def test_rows_outside_the_sequences_are_untouched(pkv):
+    rng = np.random.default_rng(514)
+    w = _random(rng, 2, 64, 16, [9, 4], [0, 16])
+    d = to_dev(w)
+    Tq = w.Tq
+    big = torch.zeros((Tq + 5, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    big[:Tq] = d["q"]
+    d["q"] = big
+    out = torch.full_like(big, 7.0)
+    run_step(pkv, w, d, out=out)
+    assert (out[Tq:] == 7.0).all()
+    assert torch.isfinite(out[:Tq].float()).all() and not (out[:Tq] == 7.0).all()
+
+
+def test_error_flags(pkv):
+    rng = np.random.default_rng(515)
+    w = _random(rng, 2, 64, 16, [9, 20], [16, 0])
+    d = to_dev(w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tables = d["tables"].clone()
+    tables[1, 0] = w.NB + 3
+    d["tables"] = tables
+    out = run_step(pkv, w, d, err=err)
+    assert int(err.item()) & pkv.FLAG_BAD_BLOCK
+    assert torch.isfinite(out.float()).all()
+    err.zero_()
+    d = to_dev(w)
+    d["cu_k"] = torch.tensor([0, 5, 25], dtype=torch.int32, device="cuda")  # k_len 5 < q_len 9
+    run_step(pkv, w, d, err=err, store=False)
+    assert int(err.item()) & pkv.FLAG_BAD_CONTEXT_LEN
+    err.zero_()
+    d = to_dev(w)
+    out = torch.empty_like(d["q"])
+    pkv.paged_prefill(d["q"], d["k_cache"], d["v_cache"], d["tables"], d["cu_q"], d["cu_k"],
+                      8, w.scale, out, err_flag=err)  # max_seqlen_q below q_len 9
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.FLAG_BAD_CONTEXT_LEN
+
+
+def test_cuda_graph_capture_and_replay(pkv):
+    w, kc, vc, ref, _ = config(0)
+    d = to_dev(w)
+    out = torch.empty_like(d["q"])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        run_step(pkv, w, d)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            pkv.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slots"])
+            pkv.paged_prefill(d["q"], d["k_cache"], d["v_cache"], d["tables"], d["cu_q"],
+                              d["cu_k"], w.max_seqlen_q, w.scale, out)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    compare(bits_host(out), ref, "graph replay")
