@@ -13,6 +13,13 @@ every context, q, out, block-table entries, context_lens, plus the store's
 rows and slots) divided by the device time per step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Two further lines measure the paths built beside the decode step (not the
+headline):
+    --kv-dtype fp8     the same decode step over FP8 (E4M3) caches
+    --path prefill     a 16384-token paged prefill step (store + causal
+                       attention through block tables), against the bf16
+                       tensor roofline
 """
 
 from __future__ import annotations
@@ -36,6 +43,11 @@ METRIC = "paged decode attention: KV GB/s & % of HBM peak; seq-steps/s (1×GB300
 WORKLOAD_IDX = 1  # the Qwen3-0.6B-shaped step
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PREFILL_METRIC = "paged prefill attention: TFLOP/s & % of bf16 tensor peak; tokens/s (1×GB300)"
+FP8_METRIC = "paged decode attention, FP8 (E4M3) KV cache: KV GB/s & % of HBM peak (1×GB300)"
+PREFILL_IDX = 1  # the 16384-token Qwen3-0.6B-shaped prefill step
+PREFILL_SOURCES = ["pkv_prefill.cuh", "pkv_prefill.h", "pkv_kernels.h", "pkv_ptx.cuh"]
 DECODE_SOURCES = ["pkv_decode.cuh", "pkv_merge.cu", "pkv_kernels.h", "pkv_ptx.cuh"]
 
 
@@ -46,7 +58,10 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--max-ctas", type=int, default=0, help="CTA cap of the decode grid (0 = one per SM)")
-    ap.add_argument("--config", type=int, default=WORKLOAD_IDX, help=argparse.SUPPRESS)
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="decode over bf16 or FP8 (E4M3) caches")
+    ap.add_argument("--path", choices=["decode", "prefill"], default="decode")
+    ap.add_argument("--config", type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -64,24 +79,35 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_source_hash() -> str:
+def load_tensor_peak():
+    """Dense bf16 TFLOP/s: (burst, sustained, source)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def decode_source_hash(sources=DECODE_SOURCES) -> str:
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "paged_kv_cache_85_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload_name: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if current."""
-    path = os.path.join(ROOT, "profiles", f"paged_decode_{workload_name}.md")
+def profiled_traffic(workload_name: str, kind: str = "paged_decode", sources=DECODE_SOURCES):
+    """DRAM bytes per launch from the committed ncu summary, if its kernel sources are current."""
+    path = os.path.join(ROOT, "profiles", f"{kind}_{workload_name}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     m_src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_src or not m_tr or m_src.group(1) != decode_source_hash():
+    if not m_src or not m_tr or m_src.group(1) != decode_source_hash(sources):
         return None
     return float(m_tr.group(1))
 
@@ -250,6 +276,96 @@ def time_oracle(w, budget_s: float):
     }
 
 
+def compact_sample(w, m):
+    """The first m sequences of a decode step with their blocks renumbered
+    0..n-1 (inputs only: block ids, tables and slots are re-indexed)."""
+    sel = np.arange(m)
+    used = []
+    for b in sel:
+        nblk = (int(w.context_lens[b]) + w.bs - 1) // w.bs
+        used.extend(int(x) for x in w.block_tables[b, :nblk])
+    ids = np.array(sorted(set(used)), np.int64)
+    remap = {int(x): i for i, x in enumerate(ids)}
+    tables = np.full((m, w.MBS), -1, np.int32)
+    for b in sel:
+        nblk = (int(w.context_lens[b]) + w.bs - 1) // w.bs
+        tables[b, :nblk] = [remap[int(x)] for x in w.block_tables[b, :nblk]]
+    slots = np.array([-1 if s < 0 else remap[int(s) // w.bs] * w.bs + int(s) % w.bs
+                      for s in w.slot_mapping[sel]], np.int64)
+    return ids, tables, slots
+
+
+def time_oracle_fp8(w, budget_s: float, k_scale: float, v_scale: float):
+    """Time the FP8 oracle (quantizing store + decode over dequantized caches)
+    on the first m sequences of the step, their blocks gathered compactly."""
+    import oracle
+
+    def run(m):
+        ids, tables, slots = compact_sample(w, m)
+        kc = oracle.quantize_bf16(w.k_cache[ids], k_scale)
+        vc = oracle.quantize_bf16(w.v_cache[ids], v_scale)
+        t0 = time.perf_counter()
+        kc, vc, _ = oracle.store_kvcache_fp8(w.k_new[:m], w.v_new[:m], kc, vc, slots, k_scale, v_scale)
+        oracle.paged_attn_decode_fp8(w.q[:m], kc, vc, tables, w.context_lens[:m], w.scale,
+                                     k_scale, v_scale)
+        return time.perf_counter() - t0
+
+    one = max(run(1), 1e-4)
+    m = int(max(1, min(w.B, budget_s / one)))
+    dt = run(m)
+    ctx = w.context_lens[:m].astype(np.int64)
+    nbytes = (int(ctx.sum()) * w.Hkv * w.D * 2 + 2 * m * w.Hq * w.D * 2
+              + int(((ctx + w.bs - 1) // w.bs).sum()) * 4 + 4 * m
+              + int((w.slot_mapping[:m] >= 0).sum()) * w.Hkv * w.D * 3 * 2 + 8 * m)
+    return {
+        "value": nbytes / dt / 1e9,
+        "unit": "GB/s",
+        "cores": 1,
+        "kind": "oracle",
+        "sample": f"FP8 store+decode of the first {m} of {w.B} sequences (all heads), fp64 C "
+                  f"oracle over dequantized caches, single thread, {dt:.1f} s",
+    }
+
+
+def prefill_sample_pairs(w, rows_per_step):
+    """(row, head) pairs spread evenly over the step's query rows, all heads."""
+    rows = np.linspace(0, w.Tq - 1, max(1, rows_per_step // w.Hq)).astype(np.int64)
+    return np.array([(r, h) for r in rows for h in range(w.Hq)], np.int32)
+
+
+def prefill_pair_flops(w, pairs):
+    """4 * D per attended key, summed over the pairs (causal keys only)."""
+    cq = w.cu_seqlens_q
+    b = np.searchsorted(cq, pairs[:, 0], side="right") - 1
+    pos = (w.k_lens[b] - w.q_lens[b]).astype(np.int64) + (pairs[:, 0] - cq[b])
+    return int(4 * w.D * (pos + 1).sum())
+
+
+def time_oracle_prefill(w, budget_s: float):
+    import oracle
+
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.store_kvcache_(w.k_new, w.v_new, kc, vc, w.slot_mapping)
+    probe = prefill_sample_pairs(w, 64)
+    t0 = time.perf_counter()
+    oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k, w.scale,
+                         pairs=probe)
+    per_pair = max(time.perf_counter() - t0, 1e-4) / len(probe)
+    pairs = prefill_sample_pairs(w, int(budget_s / per_pair))
+    t0 = time.perf_counter()
+    oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k, w.scale,
+                         pairs=pairs)
+    dt = time.perf_counter() - t0
+    return {
+        "value": prefill_pair_flops(w, pairs) / dt / 1e12,
+        "unit": "TFLOP/s",
+        "cores": 1,
+        "kind": "oracle",
+        "sample": f"causal attention of {len(pairs)} (token, head) rows spread over the "
+                  f"{w.Tq}-token step, fp64 C oracle, single thread, {dt:.1f} s",
+    }
+
+
 # ----------------------------------------------------------------- our arm
 
 
@@ -266,8 +382,10 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     pkv.load_library()
 
-    w = wl.config_workload(args.config)
-    step_bytes = w.decode_bytes() + w.store_bytes()
+    w = wl.config_workload(WORKLOAD_IDX if args.config is None else args.config)
+    fp8 = args.kv_dtype == "fp8"
+    eb = 1 if fp8 else 2
+    step_bytes = w.decode_bytes(eb) + w.store_bytes(eb)
 
     def bf(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
@@ -277,18 +395,45 @@ def run_ours(args):
                 lens=torch.from_numpy(w.context_lens))
     d = {k: v.to(dev) for k, v in host.items()}
     kc, vc = bf(w.k_cache).to(dev), bf(w.v_cache).to(dev)
+    k_scale = v_scale = 1.0
+    if fp8:
+        # per-tensor scales amax / 448 (the largest E4M3 value); the caches are
+        # quantized on the device by the library's own FP8 store
+        k_scale = max(float(kc.float().abs().amax()), float(d["kn"].float().abs().amax())) / 448.0
+        v_scale = max(float(vc.float().abs().amax()), float(d["vn"].float().abs().amax())) / 448.0
+        n_slots = w.NB * w.bs
+        kc8 = torch.empty(kc.shape, dtype=torch.uint8, device=dev)
+        vc8 = torch.empty_like(kc8)
+        pkv.store_kvcache_fp8(kc.view(n_slots, w.Hkv, w.D), vc.view(n_slots, w.Hkv, w.D), kc8, vc8,
+                              torch.arange(n_slots, dtype=torch.int64, device=dev), k_scale, v_scale)
+        torch.cuda.synchronize(dev)
+        del kc, vc
+        kc, vc = kc8, vc8
     out = torch.empty_like(d["q"])
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(dev)
     ws_bytes = pkv.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, w.MBS, w.bs, args.max_ctas)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
+    def store_call(kn, vn, slots):
+        if fp8:
+            pkv.store_kvcache_fp8(kn, vn, kc, vc, slots, k_scale, v_scale, err_flag=err)
+        else:
+            pkv.store_kvcache(kn, vn, kc, vc, slots, err_flag=err)
+
+    def attn_call(q, tables, lens):
+        if fp8:
+            pkv.paged_attn_decode_fp8(q, kc, vc, tables, lens, w.scale, k_scale, v_scale, out,
+                                      max_ctas=args.max_ctas, workspace=ws, err_flag=err)
+        else:
+            pkv.paged_attn_decode(q, kc, vc, tables, lens, w.scale, out,
+                                  max_ctas=args.max_ctas, workspace=ws, err_flag=err)
+
     def attn():
-        pkv.paged_attn_decode(d["q"], kc, vc, d["tables"], d["lens"], w.scale, out,
-                              max_ctas=args.max_ctas, workspace=ws, err_flag=err)
+        attn_call(d["q"], d["tables"], d["lens"])
 
     def step():
-        pkv.store_kvcache(d["kn"], d["vn"], kc, vc, d["slots"], err_flag=err)
+        store_call(d["kn"], d["vn"], d["slots"])
         attn()
 
     launches_per_step = (1 if w.N > 0 else 0) + 2
@@ -341,9 +486,8 @@ def run_ours(args):
 
         def e2e_step():
             dev_pack.copy_(host_pack, non_blocking=True)
-            pkv.store_kvcache(dev_views["kn"], dev_views["vn"], kc, vc, dev_views["slots"], err_flag=err)
-            pkv.paged_attn_decode(dev_views["q"], kc, vc, dev_views["tables"], dev_views["lens"],
-                                  w.scale, out, max_ctas=args.max_ctas, workspace=ws, err_flag=err)
+            store_call(dev_views["kn"], dev_views["vn"], dev_views["slots"])
+            attn_call(dev_views["q"], dev_views["tables"], dev_views["lens"])
             out_h.copy_(out, non_blocking=True)
 
         for _ in range(3):
@@ -366,7 +510,7 @@ def run_ours(args):
     ms_step = ms_total / args.steps
     value = job_throughput(step_bytes, world, ms_step)
     peak, peak_src = load_peaks()
-    achieved = w.decode_bytes() / (ms_attn * 1e-3) / 1e9
+    achieved = w.decode_bytes(eb) / (ms_attn * 1e-3) / 1e9
 
     if rank != 0:
         if dist is not None:
@@ -375,10 +519,10 @@ def run_ours(args):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle(w, budget_s=12.0)
+        cpu = time_oracle_fp8(w, 12.0, k_scale, v_scale) if fp8 else time_oracle(w, budget_s=12.0)
 
     line = {
-        "metric": METRIC,
+        "metric": FP8_METRIC if fp8 else METRIC,
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
@@ -388,15 +532,17 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)",
+        "dtype": "fp8-e4m3 KV (e4m3/f16 MMA, fp32 accumulate)" if fp8 else "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)" +
+                (", caches quantized to E4M3 with per-tensor amax/448 scales" if fp8 else ""),
         "config": {
-            "workload": w.name,
+            "workload": w.name + ("_fp8" if fp8 else ""),
             "num_seqs": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
             "block_size": w.bs, "context_lens": "uniform [128, 4096]",
             "num_blocks": w.NB, "max_blocks_per_seq": w.MBS,
             "new_tokens_per_step": w.N, "max_ctas": args.max_ctas or "one per SM",
-            "step_bytes": step_bytes, "kv_bytes": w.kv_bytes(),
+            "step_bytes": step_bytes, "kv_bytes": w.kv_bytes(eb),
+            "kv_cache_dtype": args.kv_dtype,
             "l2": "inputs larger than L2 (no flush)",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
@@ -415,8 +561,8 @@ def run_ours(args):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
-            "traffic": profiled_traffic(w.name),
-            "algorithmic_bytes_per_launch": w.decode_bytes(),
+            "traffic": profiled_traffic(w.name, "paged_decode_fp8" if fp8 else "paged_decode"),
+            "algorithmic_bytes_per_launch": w.decode_bytes(eb),
             "us_per_launch": round(ms_attn * 1e3, 2),
         },
         "e2e": {
@@ -438,6 +584,164 @@ def run_ours(args):
     return line
 
 
+def run_ours_prefill(args):
+    import torch
+
+    import paged_kv_cache_85_gb300 as pkv
+    from paged_kv_cache_85_gb300 import workload as wl
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+
+    w = wl.prefill_config_workload(PREFILL_IDX if args.config is None else args.config)
+    flops = w.flops()
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    host = dict(q=bf(w.q), kn=bf(w.k_new), vn=bf(w.v_new),
+                slots=torch.from_numpy(w.slot_mapping), tables=torch.from_numpy(w.block_tables),
+                cu_q=torch.from_numpy(w.cu_seqlens_q), cu_k=torch.from_numpy(w.cu_seqlens_k))
+    d = {k: v.to(dev) for k, v in host.items()}
+    kc, vc = bf(w.k_cache).to(dev), bf(w.v_cache).to(dev)
+    out = torch.empty_like(d["q"])
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def run(v):
+        pkv.store_kvcache(v["kn"], v["vn"], kc, vc, v["slots"], err_flag=err)
+        pkv.paged_prefill(v["q"], kc, vc, v["tables"], v["cu_q"], v["cu_k"], w.max_seqlen_q,
+                          w.scale, out, err_flag=err)
+
+    def attn():
+        pkv.paged_prefill(d["q"], kc, vc, d["tables"], d["cu_q"], d["cu_k"], w.max_seqlen_q,
+                          w.scale, out, err_flag=err)
+
+    clocks = ClockSampler(dev.index)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            run(d)
+        torch.cuda.synchronize(dev)
+        clocks.start()
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            for _ in range(5):
+                run(d)
+            torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            run(d)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        ms_total = e0.elapsed_time(e1)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            attn()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_attn = a0.elapsed_time(a1) / args.steps
+        host_pack, dev_views, _dev_pack = stage_inputs(host, dev)
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = host_pack.numel()
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            _dev_pack.copy_(host_pack, non_blocking=True)
+            run(dev_views)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        x1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = x0.elapsed_time(x1) / args.steps
+    clk = clocks.stop()
+    flags = int(err.item())
+    ms_total = reduce_max(ms_total, dist, dev)
+    ms_attn = reduce_max(ms_attn, dist, dev)
+    ms_e2e = reduce_max(ms_e2e, dist, dev)
+    ms_step = ms_total / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    peak, peak_sus, peak_src = load_tensor_peak()
+    achieved = flops / (ms_attn * 1e-3) / 1e12
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle_prefill(w, budget_s=12.0)
+    line = {
+        "metric": PREFILL_METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks, cached prefixes)",
+        "config": {
+            "workload": w.name, "num_seqs": w.B, "new_tokens": w.Tq,
+            "q_lens": sorted(set(int(x) for x in w.q_lens))[:8],
+            "cached_lens": [int(x) for x in (w.k_lens - w.q_lens)][:16],
+            "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs,
+            "causal_flops": flops, "kv_bytes": w.kv_bytes(),
+            "l2": "q + K/V + out per step exceed L2 (no flush)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "us_per_step": round(ms_step * 1e3, 2),
+        "tokens_per_s": round(world * w.Tq / (ms_step * 1e-3), 1),
+        "roofline": {
+            "kernel": "paged_prefill_kernel",
+            "bound": "tensor",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": (f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst; sustained "
+                            f"{peak_sus})"),
+            "traffic": profiled_traffic(w.name, "paged_prefill", PREFILL_SOURCES),
+            "algorithmic_flops_per_launch": flops,
+            "us_per_launch": round(ms_attn * 1e3, 2),
+        },
+        "e2e": {
+            "value": round(world * flops / (ms_e2e * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "us_per_step": round(ms_e2e * 1e3, 2),
+        },
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "device_error_flags": flags,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
 # ----------------------------------------------------------- reference arm
 
 
@@ -448,7 +752,7 @@ def run_reference(args):
         return None
     from paged_kv_cache_85_gb300 import workload as wl
 
-    w = wl.config_workload(args.config)
+    w = wl.config_workload(WORKLOAD_IDX if args.config is None else args.config)
     kc, vc = w.k_cache.copy(), w.v_cache.copy()
     t0 = time.perf_counter()
     oracle_sample(w, [0], kc, vc)
@@ -491,8 +795,60 @@ def run_reference(args):
     return line
 
 
+def run_reference_prefill(args):
+    """The oracle on a bounded sample of the prefill step per timed step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    from paged_kv_cache_85_gb300 import workload as wl
+
+    w = wl.prefill_config_workload(PREFILL_IDX if args.config is None else args.config)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.store_kvcache_(w.k_new, w.v_new, kc, vc, w.slot_mapping)
+    probe = prefill_sample_pairs(w, 64)
+    t0 = time.perf_counter()
+    oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k, w.scale,
+                         pairs=probe)
+    per_pair = max(time.perf_counter() - t0, 1e-4) / len(probe)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    pairs = prefill_sample_pairs(w, max(w.Hq, int(budget / per_pair)))
+
+    def one():
+        oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k,
+                             w.scale, pairs=pairs)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    value = prefill_pair_flops(w, pairs) * args.steps / dt / 1e12
+    sample = (f"each step: causal attention of {len(pairs)} (token, head) rows spread over the "
+              f"{w.Tq}-token step, fp64 C oracle, single thread")
+    line = {
+        "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks, cached prefixes)",
+        "config": {"workload": w.name, "num_seqs": w.B, "new_tokens": w.Tq, "q_heads": w.Hq,
+                   "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.path == "prefill":
+        return run_reference_prefill(args) if args.impl == "reference" else run_ours_prefill(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -45,19 +45,6 @@ struct DecodeParams {
     float v_scale;                // FP8 caches: dequant scale of V (1 for bf16)
 };
 
-struct PrefillParams {
-    const uint16_t *q;            // bf16 [Tq, Hq, D]: the sequences' new tokens, concatenated
-    uint16_t *out;                // bf16 [Tq, Hq, D]
-    const int32_t *block_tables;  // [B, MBS]
-    const int32_t *cu_q;          // [B + 1] boundaries of the new tokens
-    const int32_t *cu_k;          // [B + 1] boundaries of the contexts (cached + new)
-    int32_t *err_flag;            // nullable
-    long long Tq;
-    int B, Hq, Hkv, MBS, bs, NB;
-    int max_q;                    // the caller's bound on q_len (sizes the grid)
-    float scale_log2;             // scale * log2(e)
-};
-
 // Host launchers (defined next to their kernels).
 cudaError_t launch_store(const void *k, const void *v, void *k_cache, void *v_cache,
                          const int64_t *slot_mapping, int64_t N, int row_bytes,
@@ -67,11 +54,5 @@ cudaError_t launch_store_fp8(const void *k, const void *v, void *k_cache, void *
                              long long n_slots, float kinv, float vinv, int32_t *err_flag,
                              cudaStream_t stream);
 cudaError_t launch_merge(int D, int G, const DecodeParams &p, cudaStream_t stream);
-cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                           const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream);
-const void *prefill_kernel(int D, int G);
-size_t prefill_smem_bytes(int D);
-constexpr int kPrefillThreads = 8 * 32;  // 7 consumer warps + 1 producer warp
-constexpr int kPrefillRows = 112;        // (token, head) rows per CTA
 
 } // namespace pkv

@@ -29,6 +29,7 @@
 #include <stdint.h>
 
 #include "pkv_kernels.h"
+#include "pkv_prefill.h"
 #include "pkv_ptx.cuh"
 
 namespace pkv {

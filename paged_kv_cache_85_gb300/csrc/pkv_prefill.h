@@ -1,0 +1,31 @@
+// Paged prefill: kernel parameters and host-side launch entry points
+// (internal; the public ABI is pkv.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct PrefillParams {
+    const uint16_t *q;            // bf16 [Tq, Hq, D]: the sequences' new tokens, concatenated
+    uint16_t *out;                // bf16 [Tq, Hq, D]
+    const int32_t *block_tables;  // [B, MBS]
+    const int32_t *cu_q;          // [B + 1] boundaries of the new tokens
+    const int32_t *cu_k;          // [B + 1] boundaries of the contexts (cached + new)
+    int32_t *err_flag;            // nullable
+    long long Tq;
+    int B, Hq, Hkv, MBS, bs, NB;
+    int max_q;                    // the caller's bound on q_len (sizes the grid)
+    float scale_log2;             // scale * log2(e)
+};
+
+cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                           const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream);
+const void *prefill_kernel(int D, int G);
+size_t prefill_smem_bytes(int D);
+constexpr int kPrefillRows = 112;  // (token, head) rows per CTA
+
+} // namespace pkv
