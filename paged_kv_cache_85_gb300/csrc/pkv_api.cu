@@ -14,7 +14,8 @@
 #include "pkv.h"
 #include "pkv_decode.cuh"
 #include "pkv_kernels.h"
-#include "pkv_prefill.cuh"
+#include "pkv_prefill.h"
+#include "pkv_prefill_tc.cuh"
 
 namespace pkv {
 #define PKV_DECLARE_SHAPE(D, NW)                                                                  \
@@ -37,18 +38,21 @@ PKV_DECLARE_SHAPE8(64, 8)
 PKV_DECLARE_SHAPE8(128, 4)
 PKV_DECLARE_SHAPE8(128, 8)
 #undef PKV_DECLARE_SHAPE8
-cudaError_t launch_prefill_d64(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                               const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream);
-cudaError_t launch_prefill_d128(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                                const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_prefill_d64(int G, const CUtensorMap *tmq, const CUtensorMap *tmk,
+                               const CUtensorMap *tmv, const PrefillParams &p, dim3 grid,
+                               size_t smem, cudaStream_t stream);
+cudaError_t launch_prefill_d128(int G, const CUtensorMap *tmq, const CUtensorMap *tmk,
+                                const CUtensorMap *tmv, const PrefillParams &p, dim3 grid,
+                                size_t smem, cudaStream_t stream);
 const void *prefill_kernel_d64(int G);
 const void *prefill_kernel_d128(int G);
 
-cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                           const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream)
+cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmq, const CUtensorMap *tmk,
+                           const CUtensorMap *tmv, const PrefillParams &p, dim3 grid, size_t smem,
+                           cudaStream_t stream)
 {
-    return D == 128 ? launch_prefill_d128(G, tmk, tmv, p, grid, smem, stream)
-                    : launch_prefill_d64(G, tmk, tmv, p, grid, smem, stream);
+    return D == 128 ? launch_prefill_d128(G, tmq, tmk, tmv, p, grid, smem, stream)
+                    : launch_prefill_d64(G, tmq, tmk, tmv, p, grid, smem, stream);
 }
 
 const void *prefill_kernel(int D, int G)
@@ -56,7 +60,7 @@ const void *prefill_kernel(int D, int G)
     return D == 128 ? prefill_kernel_d128(G) : prefill_kernel_d64(G);
 }
 
-size_t prefill_smem_bytes(int D) { return prefill_smem_layout(D).total; }
+size_t prefill_smem_bytes(int D) { return tc_smem_layout(D).total; }
 
 const void *decode_kernel(int D, int NW, int G, bool f8)
 {
@@ -210,6 +214,25 @@ pkv_status make_cache_map(CUtensorMap *map, const void *cache, long long tokens,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+// Prefill queries q [Tq, Hq, D] bf16 as 4-D (64, D/64, Hq, Tq) like the cache;
+// box 64 x 1 x G x 128/G: one 128-row (token, head) tile half per copy.
+pkv_status make_q_map(CUtensorMap *map, const void *q, long long Tq, int Hq, int D, int G)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc)
+        return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[4] = {64, (cuuint64_t)(D / 64), (cuuint64_t)Hq, (cuuint64_t)Tq};
+    cuuint64_t strides[3] = {128, (cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)G, (cuuint32_t)(pkv::kPrefillRows / G)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed (%d)", (int)r);
     return PKV_OK;
 }
 
@@ -592,11 +615,13 @@ pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_c
             set = true;
         }
     }
-    CUtensorMap tmk, tmv;
+    CUtensorMap tmq, tmk, tmv;
     const long long tokens = (long long)NB * bs;
     if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D)) != PKV_OK)
         return ps;
     if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D)) != PKV_OK)
+        return ps;
+    if ((ps = make_q_map(&tmq, q, Tq, Hq, D, G)) != PKV_OK)
         return ps;
     pkv::PrefillParams p;
     p.q = static_cast<const uint16_t *>(q);
@@ -614,8 +639,8 @@ pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_c
     p.NB = (int)NB;
     p.max_q = max_seqlen_q;
     p.scale_log2 = scale * 1.4426950408889634f;
-    cudaError_t e = pkv::launch_prefill(D, G, &tmk, &tmv, p, dim3((unsigned)tiles, Hkv, B), smem,
-                                        static_cast<cudaStream_t>(stream));
+    cudaError_t e = pkv::launch_prefill(D, G, &tmq, &tmk, &tmv, p, dim3((unsigned)tiles, Hkv, B),
+                                        smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return fail(PKV_ERR_CUDA, "paged_prefill launch: %s", cudaGetErrorString(e));
     return PKV_OK;

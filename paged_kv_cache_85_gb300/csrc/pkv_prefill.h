@@ -22,10 +22,12 @@ struct PrefillParams {
     float scale_log2;             // scale * log2(e)
 };
 
-cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                           const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmq, const CUtensorMap *tmk,
+                           const CUtensorMap *tmv, const PrefillParams &p, dim3 grid, size_t smem,
+                           cudaStream_t stream);
 const void *prefill_kernel(int D, int G);
 size_t prefill_smem_bytes(int D);
-constexpr int kPrefillRows = 112;  // (token, head) rows per CTA
+constexpr int kPrefillRows = 128;  // (token, head) rows per CTA
+constexpr int kPrefillThreads = 6 * 32;
 
 } // namespace pkv

@@ -1,14 +1,15 @@
-// Instantiations of the paged prefill kernel, head_dim 64, G = 1, 2, 4, 8.
-#include "pkv_prefill.cuh"
+// Instantiations of the paged prefill kernel (tcgen05), head_dim 64, G = 1, 2, 4, 8.
+#include "pkv_prefill_tc.cuh"
 
 namespace pkv {
 
-cudaError_t launch_prefill_d64(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                               const PrefillParams &p, dim3 grid, size_t smem, cudaStream_t stream)
+cudaError_t launch_prefill_d64(int G, const CUtensorMap *tmq, const CUtensorMap *tmk,
+                               const CUtensorMap *tmv, const PrefillParams &p, dim3 grid,
+                               size_t smem, cudaStream_t stream)
 {
-    return launch_prefill_d<64>(G, tmk, tmv, p, grid, smem, stream);
+    return launch_prefill_tc_d<64>(G, tmq, tmk, tmv, p, grid, smem, stream);
 }
 
-const void *prefill_kernel_d64(int G) { return prefill_kernel_d<64>(G); }
+const void *prefill_kernel_d64(int G) { return prefill_tc_kernel_d<64>(G); }
 
 } // namespace pkv

@@ -1,0 +1,418 @@
+// Paged prefill attention on the 5th-generation tensor cores (tcgen05/TMEM).
+//
+// Same operation as paged_prefill_kernel (MinivLLM guide §4.5 prepare_prefill;
+// causal: new token i of a sequence sits at position k_len - q_len + i and
+// attends to positions 0 .. that one, K/V read through the block table).
+//
+// One CTA per (tile of 128 (token, head-in-group) rows, KV head, sequence);
+// two CTAs per SM, so one CTA's softmax overlaps the other's MMAs.  Warps:
+//   0..3  softmax: thread t owns row t (TMEM lane t) -- no shuffles
+//   4     producer: TMA of the Q tile once, then 64-key K/V tiles (four
+//         16-token boxes resolved through the block table) into a 2-stage ring
+//   5     MMA: allocates 256 TMEM columns; one lane issues
+//           S_j = Q K_j^T    (SS, K-major 128-byte-swizzled operands, M=128
+//                             N=64, into one of two S buffers), and
+//           O  += P_j V_j    (P from TMEM, V MN-major from shared memory,
+//                             N=D), P split into bf16 hi + lo parts.
+// TMEM columns: O in [0, D); S buffers at 128 and 192 (64 f32 columns each);
+// P_j overwrites its S buffer (hi in the first 32 columns, lo in the next 32).
+// The running max moves only when a row's tile max exceeds it by more than
+// 2^8 (then that warp rescales its O rows in TMEM after the previous P.V has
+// completed).  V rows past k_len or in unloaded boxes are zeroed in shared
+// memory before P.V (their weight is 0, and 0 * NaN would be NaN).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv_kernels.h"
+#include "pkv_prefill.h"
+#include "pkv_ptx.cuh"
+#include "pkv_tc.cuh"
+
+namespace pkv {
+
+constexpr int kTcRows = 128;            // query rows per CTA (MMA M)
+constexpr int kTcKeys = 64;             // keys per K/V tile (MMA N of S)
+constexpr int kTcStages = 2;            // K/V ring depth
+constexpr int kTcThreads = 6 * 32;
+constexpr uint32_t kTcCols = 256;       // TMEM columns per CTA
+constexpr uint32_t kTcSCol = 128;       // first S buffer column
+
+struct TcSmem {
+    size_t q, kv, bars, meta, slot, total;
+};
+
+__host__ __device__ inline TcSmem tc_smem_layout(int D)
+{
+    TcSmem L;
+    size_t o = 0;
+    L.q = o;  // [D/64 halves][128 rows][128 B]
+    o += (size_t)(D / 64) * kTcRows * 128;
+    L.kv = o;  // per stage: K [D/64][64 keys][128 B], then V alike
+    o += (size_t)kTcStages * 2 * (D / 64) * kTcKeys * 128;
+    L.bars = o;  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, mma_done
+    o += 8 * (1 + 2 * kTcStages + 2 + 2 + 2);
+    L.meta = o;
+    o += 4 * kTcStages;
+    L.slot = o;
+    o += 16;
+    L.total = align_up(o, 16) + 1024;
+    return L;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq,
+                            const __grid_constant__ CUtensorMap tmk,
+                            const __grid_constant__ CUtensorMap tmv, const PrefillParams p)
+{
+    constexpr int TPC = kTcRows / G;                  // query tokens per CTA
+    constexpr int HALVES = D / 64;
+    constexpr uint32_t kQHalf = kTcRows * 128;        // 16 KB
+    constexpr uint32_t kTileHalf = kTcKeys * 128;     // 8 KB
+    constexpr uint32_t kTile = HALVES * kTileHalf;    // one K (or V) tile
+    constexpr uint32_t kBoxBytes = kBox * D * 2;
+    constexpr unsigned FULL = 0xffffffffu;
+    constexpr float kLazy = 8.f;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const TcSmem L = tc_smem_layout(D);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *q_full = bars;
+    uint64_t *kv_full = bars + 1;
+    uint64_t *kv_empty = kv_full + kTcStages;
+    uint64_t *s_full = kv_empty + kTcStages;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_done = p_full + 2;
+    uint64_t *mma_done = o_done + 1;
+    uint32_t *meta = reinterpret_cast<uint32_t *>(smem + L.meta);
+    uint32_t *slot = reinterpret_cast<uint32_t *>(smem + L.slot);
+    uint8_t *sQ = smem + L.q;
+    uint8_t *sKV = smem + L.kv;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.z, kvh = blockIdx.y;
+    const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;  // the longest tiles start first
+
+    grid_launch_dependents();
+    const int cq0 = __ldg(p.cu_q + b), cq1 = __ldg(p.cu_q + b + 1);
+    const int ck0 = __ldg(p.cu_k + b), ck1 = __ldg(p.cu_k + b + 1);
+    const int q_len = cq1 - cq0, k_len = ck1 - ck0;
+    const bool sane = cq0 >= 0 && q_len >= 0 && (long long)cq1 <= p.Tq && k_len >= q_len &&
+                      k_len <= p.MBS * p.bs && q_len <= p.max_q;
+    if (!sane) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0)
+            flag_error(p.err_flag, 0x4 /* PKV_FLAG_BAD_CONTEXT_LEN */);
+        return;
+    }
+    const int tok0 = tile * TPC;
+    if (tok0 >= q_len)
+        return;
+    const int base = k_len - q_len;  // position of new token 0
+    const int last_pos = base + min(q_len, tok0 + TPC) - 1;
+    const int nkt = last_pos / kTcKeys + 1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kTcStages; s++) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
+        }
+        mbar_init(o_done, 1);
+        mbar_init(mma_done, 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 5) {
+        tc::alloc(smem_u32(slot), kTcCols);
+        tc::relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *slot;
+    const uint32_t tO = tmem, tS0 = tmem + kTcSCol;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensormap(&tmq);
+            prefetch_tensormap(&tmk);
+            prefetch_tensormap(&tmv);
+        }
+        const int32_t *table = p.block_tables + (size_t)b * p.MBS;
+        grid_dependency_wait();  // K/V may have just been written by store_kvcache
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, HALVES * kQHalf);
+#pragma unroll
+            for (int h = 0; h < HALVES; h++)
+                tma_load_4d(sQ + h * kQHalf, &tmq, 0, h, kvh * G, cq0 + tok0, q_full);
+        }
+        bool ok = true;
+        int issued = 0;
+        for (int j = 0; j < nkt && ok; j++) {
+            const int s = j % kTcStages;
+            if (!__all_sync(FULL, mbar_wait(&kv_empty[s], ((j / kTcStages) & 1) ^ 1))) {
+                ok = false;
+                break;
+            }
+            const int key0 = j * kTcKeys + lane * kBox;
+            bool loaded = false;
+            int row = 0;
+            if (lane < kTcKeys / kBox && key0 < k_len) {
+                const int blk = __ldg(table + key0 / p.bs);
+                loaded = blk >= 0 && blk < p.NB;
+                if (!loaded)
+                    flag_error(p.err_flag, 0x2 /* PKV_FLAG_BAD_BLOCK */);
+                row = blk * p.bs + key0 % p.bs;
+            }
+            const uint32_t mask = __ballot_sync(FULL, loaded);
+            if (lane == 0) {
+                meta[s] = mask;
+                mbar_arrive_expect_tx(&kv_full[s], (uint32_t)__popc(mask) * 2u * kBoxBytes);
+            }
+            __syncwarp();
+            if (loaded) {
+                uint8_t *kd = sKV + (size_t)s * 2 * kTile + lane * (kBox * 128);
+#pragma unroll
+                for (int h = 0; h < HALVES; h++) {
+                    tma_load_4d(kd + h * kTileHalf, &tmk, 0, h, kvh, row, &kv_full[s]);
+                    tma_load_4d(kd + kTile + h * kTileHalf, &tmv, 0, h, kvh, row, &kv_full[s]);
+                }
+            }
+            issued = j + 1;
+        }
+        if (!ok && lane == 0)
+            flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
+        // copies still in flight land before the CTA may exit
+        if (lane == 0) {
+            mbar_wait(q_full, 0);
+            for (int j = max(0, issued - kTcStages); j < issued; j++)
+                mbar_wait(&kv_full[j % kTcStages], (j / kTcStages) & 1);
+        }
+    } else if (warp == 5) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            bool ok = mbar_wait(q_full, 0);
+            const uint32_t qa = smem_u32(sQ);
+            const uint32_t idS = tc::idesc_bf16(kTcRows, kTcKeys, false);
+            const uint32_t idO = tc::idesc_bf16(kTcRows, D, true);
+            auto issue_s = [&](int j) {
+                const int s = j % kTcStages;
+                const uint32_t ka = smem_u32(sKV + (size_t)s * 2 * kTile);
+                const uint32_t dst = tS0 + (uint32_t)(j & 1) * kTcKeys;
+#pragma unroll
+                for (int k = 0; k < D / 16; k++) {
+                    const uint32_t off = (uint32_t)(k >> 2) * kQHalf + (uint32_t)(k & 3) * 32;
+                    const uint32_t offk = (uint32_t)(k >> 2) * kTileHalf + (uint32_t)(k & 3) * 32;
+                    tc::mma_ss(dst, tc::smem_desc(qa + off, 16, 1024),
+                               tc::smem_desc(ka + offk, 16, 1024), idS, k > 0);
+                }
+                tc::commit(smem_u32(&s_full[j & 1]));
+            };
+            if (ok && (ok = mbar_wait(&kv_full[0], 0)))
+                issue_s(0);
+            for (int j = 0; j < nkt && ok; j++) {
+                if (j + 1 < nkt) {
+                    if (!(ok = mbar_wait(&kv_full[(j + 1) % kTcStages], ((j + 1) / kTcStages) & 1)))
+                        break;
+                    issue_s(j + 1);
+                }
+                if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1)))
+                    break;
+                tc::fence_after();
+                const int s = j % kTcStages;
+                const uint32_t va = smem_u32(sKV + (size_t)s * 2 * kTile + kTile);
+                const uint32_t pS = tS0 + (uint32_t)(j & 1) * kTcKeys;
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; kk++) {
+                    const uint64_t dv = tc::smem_desc(va + kk * 16 * 128, kTileHalf, 1024);
+                    tc::mma_ts(tO, pS + 8 * kk, dv, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_ts(tO, pS + 32 + 8 * kk, dv, idO, 1u);
+                }
+                tc::commit(smem_u32(&kv_empty[s]));
+                tc::commit(smem_u32(o_done));
+            }
+            if (!ok)
+                flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
+            // every MMA issued has completed before TMEM is released
+            tc::commit(smem_u32(mma_done));
+            mbar_wait(mma_done, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------- softmax
+        const int r = threadIdx.x;            // row = TMEM lane
+        const int tok = tok0 + r / G, g = r % G;
+        const bool valid = tok < q_len;
+        const int pos = base + tok;
+        const uint32_t tl = (uint32_t)(32 * warp) << 16;
+        grid_dependency_wait();
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkt; j++) {
+            const int s = j % kTcStages;
+            const uint32_t tS = tS0 + (uint32_t)(j & 1) * kTcKeys;
+            ok = __all_sync(FULL, mbar_wait(&s_full[j & 1], (j >> 1) & 1) &&
+                                      mbar_wait(&kv_full[s], (j / kTcStages) & 1));
+            if (!ok)
+                break;
+            tc::fence_after();
+            const uint32_t mask = meta[s];
+            float x[kTcKeys];
+            {
+                uint32_t ra[32];
+                tc::ld32(tS + tl, ra);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i++)
+                    x[i] = __uint_as_float(ra[i]) * p.scale_log2;
+                tc::ld32(tS + tl + 32, ra);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i++)
+                    x[32 + i] = __uint_as_float(ra[i]) * p.scale_log2;
+            }
+            const int key_base = j * kTcKeys;
+            if (mask != 0xFu || key_base + kTcKeys - 1 > pos) {
+#pragma unroll
+                for (int i = 0; i < kTcKeys; i++)
+                    if (key_base + i > pos || !((mask >> (i / kBox)) & 1u))
+                        x[i] = -INFINITY;
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int i = 1; i < kTcKeys; i++)
+                mx = fmaxf(mx, x[i]);
+            if (__any_sync(FULL, mx > m + kLazy)) {
+                const float mn = fmaxf(m, mx);
+                const float alpha = mn == -INFINITY ? 1.f : fast_exp2(m - mn);
+                if (j > 0) {
+                    // O holds P_0..P_{j-1} V: rescale once the last P.V completed
+                    if (!(ok = __all_sync(FULL, mbar_wait(o_done, (j - 1) & 1))))
+                        break;
+                    tc::fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; c++) {
+                        uint32_t ro[32];
+                        tc::ld32(tO + tl + 32 * c, ro);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i++)
+                            ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+                        tc::st32(tO + tl + 32 * c, ro);
+                    }
+                    tc::wait_st();
+                }
+                l *= alpha;
+                m = mn;
+            }
+            const float mu = m == -INFINITY ? 0.f : m;
+            {
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    const float p0 = fast_exp2(x[2 * i] - mu), p1 = fast_exp2(x[2 * i + 1] - mu);
+                    l += p0 + p1;
+                    hi[i] = pack_bf16x2(p0, p1);
+                    const float2 h = bf16x2_to_float2(hi[i]);
+                    lo[i] = pack_bf16x2(p0 - h.x, p1 - h.y);
+                }
+                tc::st32(tS + tl, hi);
+                tc::st32(tS + tl + 32, lo);
+                tc::wait_st();
+            }
+            // V rows past k_len or in unloaded boxes: zero them (all four warps)
+            if (mask != 0xFu || key_base + kTcKeys > k_len) {
+                uint8_t *vt = sKV + (size_t)s * 2 * kTile + kTile;
+                for (int it = r; it < HALVES * kTcKeys * 8; it += 128) {
+                    const int h = it / (kTcKeys * 8), kr = (it / 8) % kTcKeys, c = it % 8;
+                    if (key_base + kr >= k_len || !((mask >> (kr / kBox)) & 1u))
+                        *reinterpret_cast<uint4 *>(vt + h * kTileHalf + kr * 128 + c * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&p_full[j & 1]);
+        }
+        if (ok)
+            ok = __all_sync(FULL, mbar_wait(o_done, (nkt - 1) & 1));
+        if (!ok) {
+            if (lane == 0)
+                flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
+        } else {
+            tc::fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint16_t *dst = p.out + ((size_t)(cq0 + tok) * p.Hq + kvh * G + g) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; c++) {
+                uint32_t ro[32];
+                tc::ld32(tO + tl + 32 * c, ro);
+                tc::wait_ld();
+                if (valid) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; i++)
+                        pk[i] = pack_bf16x2(__uint_as_float(ro[2 * i]) * inv,
+                                            __uint_as_float(ro[2 * i + 1]) * inv);
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc::fence_after();
+        tc::dealloc(tmem, kTcCols);
+    }
+}
+
+template <int D>
+inline cudaError_t launch_prefill_tc_d(int G, const CUtensorMap *tmq, const CUtensorMap *tmk,
+                                       const CUtensorMap *tmv, const PrefillParams &p, dim3 grid,
+                                       size_t smem, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    switch (G) {
+    case 1: return cudaLaunchKernelEx(&cfg, paged_prefill_tc_kernel<D, 1>, *tmq, *tmk, *tmv, p);
+    case 2: return cudaLaunchKernelEx(&cfg, paged_prefill_tc_kernel<D, 2>, *tmq, *tmk, *tmv, p);
+    case 4: return cudaLaunchKernelEx(&cfg, paged_prefill_tc_kernel<D, 4>, *tmq, *tmk, *tmv, p);
+    case 8: return cudaLaunchKernelEx(&cfg, paged_prefill_tc_kernel<D, 8>, *tmq, *tmk, *tmv, p);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int D> inline const void *prefill_tc_kernel_d(int G)
+{
+    switch (G) {
+    case 1: return reinterpret_cast<const void *>(&paged_prefill_tc_kernel<D, 1>);
+    case 2: return reinterpret_cast<const void *>(&paged_prefill_tc_kernel<D, 2>);
+    case 4: return reinterpret_cast<const void *>(&paged_prefill_tc_kernel<D, 4>);
+    case 8: return reinterpret_cast<const void *>(&paged_prefill_tc_kernel<D, 8>);
+    default: return nullptr;
+    }
+}
+
+} // namespace pkv
