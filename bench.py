@@ -47,7 +47,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_METRIC = "paged prefill attention: TFLOP/s & % of bf16 tensor peak; tokens/s (1×GB300)"
 FP8_METRIC = "paged decode attention, FP8 (E4M3) KV cache: KV GB/s & % of HBM peak (1×GB300)"
 PREFILL_IDX = 1  # the 16384-token Qwen3-0.6B-shaped prefill step
-PREFILL_SOURCES = ["pkv_prefill.cuh", "pkv_prefill.h", "pkv_kernels.h", "pkv_ptx.cuh"]
+PREFILL_SOURCES = ["pkv_prefill_tc.cuh", "pkv_prefill.h", "pkv_tc.cuh", "pkv_kernels.h", "pkv_ptx.cuh"]
 DECODE_SOURCES = ["pkv_decode.cuh", "pkv_merge.cu", "pkv_kernels.h", "pkv_ptx.cuh"]
 
 
@@ -93,8 +93,11 @@ def load_tensor_peak():
 def decode_source_hash(sources=DECODE_SOURCES) -> str:
     h = hashlib.sha256()
     for name in sources:
-        with open(os.path.join(ROOT, "paged_kv_cache_85_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        path = os.path.join(ROOT, "paged_kv_cache_85_gb300", "csrc", name)
+        h.update(name.encode())
+        if os.path.exists(path):
+            with open(path, "rb") as f:
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 

@@ -7,8 +7,11 @@
 // One CTA per (tile of 128 (token, head-in-group) rows, KV head, sequence);
 // two CTAs per SM, so one CTA's softmax overlaps the other's MMAs.  Warps:
 //   0..3  softmax: thread t owns row t (TMEM lane t) -- no shuffles
-//   4     producer: TMA of the Q tile once, then 64-key K/V tiles (four
-//         16-token boxes resolved through the block table) into a 2-stage ring
+//   4     producer: TMA of the Q tile once, then 64-key K and V tiles (four
+//         16-token boxes each, resolved through the block table) into two
+//         separate 2-stage rings, lanes 0-3 for K and 4-7 for V: a K tile is
+//         released as soon as its S MMA completes, so the next K tiles load
+//         while the softmax runs, and V only has to arrive by its P.V
 //   5     MMA: allocates 256 TMEM columns; one lane issues
 //           S_j = Q K_j^T    (SS, K-major 128-byte-swizzled operands, M=128
 //                             N=64, into one of two S buffers), and
@@ -41,7 +44,7 @@ constexpr uint32_t kTcCols = 256;       // TMEM columns per CTA
 constexpr uint32_t kTcSCol = 128;       // first S buffer column
 
 struct TcSmem {
-    size_t q, kv, bars, meta, slot, total;
+    size_t q, kv, bars, slot, total;
 };
 
 __host__ __device__ inline TcSmem tc_smem_layout(int D)
@@ -52,10 +55,9 @@ __host__ __device__ inline TcSmem tc_smem_layout(int D)
     o += (size_t)(D / 64) * kTcRows * 128;
     L.kv = o;  // per stage: K [D/64][64 keys][128 B], then V alike
     o += (size_t)kTcStages * 2 * (D / 64) * kTcKeys * 128;
-    L.bars = o;  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, mma_done
-    o += 8 * (1 + 2 * kTcStages + 2 + 2 + 2);
-    L.meta = o;
-    o += 4 * kTcStages;
+    L.bars = o;  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
+                 // o_done, mma_done
+    o += 8 * (1 + 4 * kTcStages + 2 + 2 + 2);
     L.slot = o;
     o += 16;
     L.total = align_up(o, 16) + 1024;
@@ -82,13 +84,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const TcSmem L = tc_smem_layout(D);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *q_full = bars;
-    uint64_t *kv_full = bars + 1;
-    uint64_t *kv_empty = kv_full + kTcStages;
-    uint64_t *s_full = kv_empty + kTcStages;
+    uint64_t *k_full = bars + 1;
+    uint64_t *k_empty = k_full + kTcStages;
+    uint64_t *v_full = k_empty + kTcStages;
+    uint64_t *v_empty = v_full + kTcStages;
+    uint64_t *s_full = v_empty + kTcStages;
     uint64_t *p_full = s_full + 2;
     uint64_t *o_done = p_full + 2;
     uint64_t *mma_done = o_done + 1;
-    uint32_t *meta = reinterpret_cast<uint32_t *>(smem + L.meta);
     uint32_t *slot = reinterpret_cast<uint32_t *>(smem + L.slot);
     uint8_t *sQ = smem + L.q;
     uint8_t *sKV = smem + L.kv;
@@ -118,8 +121,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < kTcStages; s++) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(&s_full[i], 1);
@@ -154,48 +159,54 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             for (int h = 0; h < HALVES; h++)
                 tma_load_4d(sQ + h * kQHalf, &tmq, 0, h, kvh * G, cq0 + tok0, q_full);
         }
+        // lanes 0-3 stream K boxes, lanes 4-7 V boxes, each group at its own pace
+        const int grp = lane >> 2, gl = lane & 3;
+        const unsigned gmask = 0xFu << (4 * grp);
+        uint64_t *full_bar = grp == 0 ? k_full : v_full;
+        uint64_t *empty_bar = grp == 0 ? k_empty : v_empty;
+        const CUtensorMap *map = grp == 0 ? &tmk : &tmv;
         bool ok = true;
         int issued = 0;
-        for (int j = 0; j < nkt && ok; j++) {
-            const int s = j % kTcStages;
-            if (!__all_sync(FULL, mbar_wait(&kv_empty[s], ((j / kTcStages) & 1) ^ 1))) {
-                ok = false;
-                break;
-            }
-            const int key0 = j * kTcKeys + lane * kBox;
-            bool loaded = false;
-            int row = 0;
-            if (lane < kTcKeys / kBox && key0 < k_len) {
-                const int blk = __ldg(table + key0 / p.bs);
-                loaded = blk >= 0 && blk < p.NB;
-                if (!loaded)
-                    flag_error(p.err_flag, 0x2 /* PKV_FLAG_BAD_BLOCK */);
-                row = blk * p.bs + key0 % p.bs;
-            }
-            const uint32_t mask = __ballot_sync(FULL, loaded);
-            if (lane == 0) {
-                meta[s] = mask;
-                mbar_arrive_expect_tx(&kv_full[s], (uint32_t)__popc(mask) * 2u * kBoxBytes);
-            }
-            __syncwarp();
-            if (loaded) {
-                uint8_t *kd = sKV + (size_t)s * 2 * kTile + lane * (kBox * 128);
-#pragma unroll
-                for (int h = 0; h < HALVES; h++) {
-                    tma_load_4d(kd + h * kTileHalf, &tmk, 0, h, kvh, row, &kv_full[s]);
-                    tma_load_4d(kd + kTile + h * kTileHalf, &tmv, 0, h, kvh, row, &kv_full[s]);
+        if (lane < 8) {
+            for (int j = 0; j < nkt; j++) {
+                const int s = j % kTcStages;
+                if (!__all_sync(gmask, mbar_wait(&empty_bar[s], ((j / kTcStages) & 1) ^ 1))) {
+                    ok = false;
+                    break;
                 }
+                const int key0 = j * kTcKeys + gl * kBox;
+                bool loaded = false;
+                int row = 0;
+                if (key0 < k_len) {
+                    const int blk = __ldg(table + key0 / p.bs);
+                    loaded = blk >= 0 && blk < p.NB;
+                    if (!loaded && grp == 0)
+                        flag_error(p.err_flag, 0x2 /* PKV_FLAG_BAD_BLOCK */);
+                    row = blk * p.bs + key0 % p.bs;
+                }
+                const uint32_t mask = (__ballot_sync(gmask, loaded) >> (4 * grp)) & 0xFu;
+                if (gl == 0)
+                    mbar_arrive_expect_tx(&full_bar[s], (uint32_t)__popc(mask) * kBoxBytes);
+                __syncwarp(gmask);
+                if (loaded) {
+                    uint8_t *dst = sKV + (size_t)s * 2 * kTile + (grp == 0 ? 0u : kTile) +
+                                   gl * (kBox * 128);
+#pragma unroll
+                    for (int h = 0; h < HALVES; h++)
+                        tma_load_4d(dst + h * kTileHalf, map, 0, h, kvh, row, &full_bar[s]);
+                }
+                issued = j + 1;
             }
-            issued = j + 1;
+            if (!ok && gl == 0)
+                flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
+            // copies still in flight land before the CTA may exit
+            if (gl == 0)
+                for (int j = max(0, issued - kTcStages); j < issued; j++)
+                    mbar_wait(&full_bar[j % kTcStages], (j / kTcStages) & 1);
         }
-        if (!ok && lane == 0)
-            flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
-        // copies still in flight land before the CTA may exit
-        if (lane == 0) {
+        if (lane == 0)
             mbar_wait(q_full, 0);
-            for (int j = max(0, issued - kTcStages); j < issued; j++)
-                mbar_wait(&kv_full[j % kTcStages], (j / kTcStages) & 1);
-        }
+        __syncwarp();
     } else if (warp == 5) {
         // ----------------------------------------------------------------- MMA
         if (lane == 0) {
@@ -215,16 +226,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                                tc::smem_desc(ka + offk, 16, 1024), idS, k > 0);
                 }
                 tc::commit(smem_u32(&s_full[j & 1]));
+                tc::commit(smem_u32(&k_empty[s]));
             };
-            if (ok && (ok = mbar_wait(&kv_full[0], 0)))
+            if (ok && (ok = mbar_wait(&k_full[0], 0)))
                 issue_s(0);
             for (int j = 0; j < nkt && ok; j++) {
                 if (j + 1 < nkt) {
-                    if (!(ok = mbar_wait(&kv_full[(j + 1) % kTcStages], ((j + 1) / kTcStages) & 1)))
+                    if (!(ok = mbar_wait(&k_full[(j + 1) % kTcStages], ((j + 1) / kTcStages) & 1)))
                         break;
                     issue_s(j + 1);
                 }
                 if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1)))
+                    break;
+                if (!(ok = mbar_wait(&v_full[j % kTcStages], (j / kTcStages) & 1)))
                     break;
                 tc::fence_after();
                 const int s = j % kTcStages;
@@ -236,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     tc::mma_ts(tO, pS + 8 * kk, dv, idO, (j > 0 || kk > 0) ? 1u : 0u);
                     tc::mma_ts(tO, pS + 32 + 8 * kk, dv, idO, 1u);
                 }
-                tc::commit(smem_u32(&kv_empty[s]));
+                tc::commit(smem_u32(&v_empty[s]));
                 tc::commit(smem_u32(o_done));
             }
             if (!ok)
@@ -253,18 +267,30 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const bool valid = tok < q_len;
         const int pos = base + tok;
         const uint32_t tl = (uint32_t)(32 * warp) << 16;
+        const int32_t *table = p.block_tables + (size_t)b * p.MBS;
         grid_dependency_wait();
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkt; j++) {
             const int s = j % kTcStages;
             const uint32_t tS = tS0 + (uint32_t)(j & 1) * kTcKeys;
-            ok = __all_sync(FULL, mbar_wait(&s_full[j & 1], (j >> 1) & 1) &&
-                                      mbar_wait(&kv_full[s], (j / kTcStages) & 1));
+            // boxes of this tile the producer loads (block ids in [0, NB)); read
+            // from the table here, not from the producer, whose K stage may
+            // already hold a later tile
+            uint32_t mask;
+            {
+                const int key0 = j * kTcKeys + (lane & 3) * kBox;
+                bool ld = false;
+                if (lane < 4 && key0 < k_len) {
+                    const int blk = __ldg(table + key0 / p.bs);
+                    ld = blk >= 0 && blk < p.NB;
+                }
+                mask = __ballot_sync(FULL, ld) & 0xFu;
+            }
+            ok = __all_sync(FULL, mbar_wait(&s_full[j & 1], (j >> 1) & 1));
             if (!ok)
                 break;
             tc::fence_after();
-            const uint32_t mask = meta[s];
             float x[kTcKeys];
             {
                 uint32_t ra[32];
@@ -330,6 +356,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
             // V rows past k_len or in unloaded boxes: zero them (all four warps)
             if (mask != 0xFu || key_base + kTcKeys > k_len) {
+                // after the V copies of this tile have landed
+                if (!(ok = __all_sync(FULL, mbar_wait(&v_full[s], (j / kTcStages) & 1))))
+                    break;
                 uint8_t *vt = sKV + (size_t)s * 2 * kTile + kTile;
                 for (int it = r; it < HALVES * kTcKeys * 8; it += 128) {
                     const int h = it / (kTcKeys * 8), kr = (it / 8) % kTcKeys, c = it % 8;
