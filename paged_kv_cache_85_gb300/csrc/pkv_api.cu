@@ -638,7 +638,8 @@ pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_c
     p.bs = bs;
     p.NB = (int)NB;
     p.max_q = max_seqlen_q;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+    p.neg_scale = scale < 0.f;
     cudaError_t e = pkv::launch_prefill(D, G, &tmq, &tmk, &tmv, p, dim3((unsigned)tiles, Hkv, B),
                                         smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)

@@ -19,7 +19,8 @@ struct PrefillParams {
     long long Tq;
     int B, Hq, Hkv, MBS, bs, NB;
     int max_q;                    // the caller's bound on q_len (sizes the grid)
-    float scale_log2;             // scale * log2(e)
+    float scale_log2;             // |scale| * log2(e)
+    int neg_scale;                // scale < 0: the score MMA negates Q
 };
 
 cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmq, const CUtensorMap *tmk,

@@ -19,6 +19,8 @@
 //                             N=D), P split into bf16 hi + lo parts.
 // TMEM columns: O in [0, D); S buffers at 128 and 192 (64 f32 columns each);
 // P_j overwrites its S buffer (hi in the first 32 columns, lo in the next 32).
+// An S MMA is issued into a buffer only after the P.V that read the P in it
+// has completed (MMAs are not ordered against each other's TMEM accesses).
 // The running max moves only when a row's tile max exceeds it by more than
 // 2^8 (then that warp rescales its O rows in TMEM after the previous P.V has
 // completed).  V rows past k_len or in unloaded boxes are zeroed in shared
@@ -38,7 +40,8 @@ namespace pkv {
 
 constexpr int kTcRows = 128;            // query rows per CTA (MMA M)
 constexpr int kTcKeys = 64;             // keys per K/V tile (MMA N of S)
-constexpr int kTcStages = 2;            // K/V ring depth
+constexpr int kTcKStages = 2;           // K ring depth
+constexpr int kTcVStages = 2;           // V ring depth
 constexpr int kTcThreads = 6 * 32;
 constexpr uint32_t kTcCols = 256;       // TMEM columns per CTA
 constexpr uint32_t kTcSCol = 128;       // first S buffer column
@@ -53,11 +56,11 @@ __host__ __device__ inline TcSmem tc_smem_layout(int D)
     size_t o = 0;
     L.q = o;  // [D/64 halves][128 rows][128 B]
     o += (size_t)(D / 64) * kTcRows * 128;
-    L.kv = o;  // per stage: K [D/64][64 keys][128 B], then V alike
-    o += (size_t)kTcStages * 2 * (D / 64) * kTcKeys * 128;
+    L.kv = o;  // K stages [D/64][64 keys][128 B], then V stages alike
+    o += (size_t)(kTcKStages + kTcVStages) * (D / 64) * kTcKeys * 128;
     L.bars = o;  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
                  // o_done, mma_done
-    o += 8 * (1 + 4 * kTcStages + 2 + 2 + 2);
+    o += 8 * (1 + 2 * kTcKStages + 2 * kTcVStages + 2 + 2 + 2);
     L.slot = o;
     o += 16;
     L.total = align_up(o, 16) + 1024;
@@ -85,16 +88,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *q_full = bars;
     uint64_t *k_full = bars + 1;
-    uint64_t *k_empty = k_full + kTcStages;
-    uint64_t *v_full = k_empty + kTcStages;
-    uint64_t *v_empty = v_full + kTcStages;
-    uint64_t *s_full = v_empty + kTcStages;
+    uint64_t *k_empty = k_full + kTcKStages;
+    uint64_t *v_full = k_empty + kTcKStages;
+    uint64_t *v_empty = v_full + kTcVStages;
+    uint64_t *s_full = v_empty + kTcVStages;
     uint64_t *p_full = s_full + 2;
     uint64_t *o_done = p_full + 2;
     uint64_t *mma_done = o_done + 1;
     uint32_t *slot = reinterpret_cast<uint32_t *>(smem + L.slot);
     uint8_t *sQ = smem + L.q;
-    uint8_t *sKV = smem + L.kv;
+    uint8_t *sK = smem + L.kv;                                   // kTcKStages K tiles
+    uint8_t *sV = sK + (size_t)kTcKStages * (D / 64) * kTcKeys * 128;  // kTcVStages V tiles
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y;
@@ -120,9 +124,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < kTcStages; s++) {
+        for (int s = 0; s < kTcKStages; s++) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < kTcVStages; s++) {
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
@@ -165,12 +171,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         uint64_t *full_bar = grp == 0 ? k_full : v_full;
         uint64_t *empty_bar = grp == 0 ? k_empty : v_empty;
         const CUtensorMap *map = grp == 0 ? &tmk : &tmv;
+        const int nst = grp == 0 ? kTcKStages : kTcVStages;
+        uint8_t *ring = grp == 0 ? sK : sV;
         bool ok = true;
         int issued = 0;
         if (lane < 8) {
             for (int j = 0; j < nkt; j++) {
-                const int s = j % kTcStages;
-                if (!__all_sync(gmask, mbar_wait(&empty_bar[s], ((j / kTcStages) & 1) ^ 1))) {
+                const int s = j % nst;
+                if (!__all_sync(gmask, mbar_wait(&empty_bar[s], ((j / nst) & 1) ^ 1))) {
                     ok = false;
                     break;
                 }
@@ -189,8 +197,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     mbar_arrive_expect_tx(&full_bar[s], (uint32_t)__popc(mask) * kBoxBytes);
                 __syncwarp(gmask);
                 if (loaded) {
-                    uint8_t *dst = sKV + (size_t)s * 2 * kTile + (grp == 0 ? 0u : kTile) +
-                                   gl * (kBox * 128);
+                    uint8_t *dst = ring + (size_t)s * kTile + gl * (kBox * 128);
 #pragma unroll
                     for (int h = 0; h < HALVES; h++)
                         tma_load_4d(dst + h * kTileHalf, map, 0, h, kvh, row, &full_bar[s]);
@@ -201,8 +208,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
             // copies still in flight land before the CTA may exit
             if (gl == 0)
-                for (int j = max(0, issued - kTcStages); j < issued; j++)
-                    mbar_wait(&full_bar[j % kTcStages], (j / kTcStages) & 1);
+                for (int j = max(0, issued - nst); j < issued; j++)
+                    mbar_wait(&full_bar[j % nst], (j / nst) & 1);
         }
         if (lane == 0)
             mbar_wait(q_full, 0);
@@ -212,11 +219,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (lane == 0) {
             bool ok = mbar_wait(q_full, 0);
             const uint32_t qa = smem_u32(sQ);
-            const uint32_t idS = tc::idesc_bf16(kTcRows, kTcKeys, false);
+            // a negative scale is applied by negating Q (bit 13 of the descriptor)
+            const uint32_t idS = tc::idesc_bf16(kTcRows, kTcKeys, false) | (p.neg_scale ? 1u << 13 : 0u);
             const uint32_t idO = tc::idesc_bf16(kTcRows, D, true);
             auto issue_s = [&](int j) {
-                const int s = j % kTcStages;
-                const uint32_t ka = smem_u32(sKV + (size_t)s * 2 * kTile);
+                const int s = j % kTcKStages;
+                const uint32_t ka = smem_u32(sK + (size_t)s * kTile);
                 const uint32_t dst = tS0 + (uint32_t)(j & 1) * kTcKeys;
 #pragma unroll
                 for (int k = 0; k < D / 16; k++) {
@@ -232,17 +240,22 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 issue_s(0);
             for (int j = 0; j < nkt && ok; j++) {
                 if (j + 1 < nkt) {
-                    if (!(ok = mbar_wait(&k_full[(j + 1) % kTcStages], ((j + 1) / kTcStages) & 1)))
+                    if (!(ok = mbar_wait(&k_full[(j + 1) % kTcKStages], ((j + 1) / kTcKStages) & 1)))
+                        break;
+                    // S_{j+1} overwrites the buffer P_{j-1} occupies: the tensor pipe
+                    // does not order P.V_{j-1}'s TMEM reads before a later MMA's
+                    // writes, so wait for P.V_{j-1} (long done, a softmax ago)
+                    if (j >= 1 && !(ok = mbar_wait(o_done, (j - 1) & 1)))
                         break;
                     issue_s(j + 1);
                 }
                 if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1)))
                     break;
-                if (!(ok = mbar_wait(&v_full[j % kTcStages], (j / kTcStages) & 1)))
+                if (!(ok = mbar_wait(&v_full[j % kTcVStages], (j / kTcVStages) & 1)))
                     break;
                 tc::fence_after();
-                const int s = j % kTcStages;
-                const uint32_t va = smem_u32(sKV + (size_t)s * 2 * kTile + kTile);
+                const int s = j % kTcVStages;
+                const uint32_t va = smem_u32(sV + (size_t)s * kTile);
                 const uint32_t pS = tS0 + (uint32_t)(j & 1) * kTcKeys;
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; kk++) {
@@ -272,7 +285,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkt; j++) {
-            const int s = j % kTcStages;
             const uint32_t tS = tS0 + (uint32_t)(j & 1) * kTcKeys;
             // boxes of this tile the producer loads (block ids in [0, NB)); read
             // from the table here, not from the producer, whose K stage may
@@ -291,31 +303,42 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             if (!ok)
                 break;
             tc::fence_after();
+            // raw scores of this row; the scale is applied inside the exp2
+            // argument (p.scale_log2 >= 0: a negative scale negates Q in the MMA)
             float x[kTcKeys];
             {
-                uint32_t ra[32];
+                uint32_t ra[32], rb[32];
                 tc::ld32(tS + tl, ra);
+                tc::ld32(tS + tl + 32, rb);
                 tc::wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; i++)
-                    x[i] = __uint_as_float(ra[i]) * p.scale_log2;
-                tc::ld32(tS + tl + 32, ra);
-                tc::wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; i++)
-                    x[32 + i] = __uint_as_float(ra[i]) * p.scale_log2;
+                for (int i = 0; i < 32; i++) {
+                    x[i] = __uint_as_float(ra[i]);
+                    x[32 + i] = __uint_as_float(rb[i]);
+                }
             }
             const int key_base = j * kTcKeys;
-            if (mask != 0xFu || key_base + kTcKeys - 1 > pos) {
+            const bool masked = mask != 0xFu || key_base + kTcKeys - 1 > pos;
+            if (masked) {
 #pragma unroll
                 for (int i = 0; i < kTcKeys; i++)
                     if (key_base + i > pos || !((mask >> (i / kBox)) & 1u))
                         x[i] = -INFINITY;
             }
-            float mx = x[0];
+            float mraw;
+            {
+                float t[8];
 #pragma unroll
-            for (int i = 1; i < kTcKeys; i++)
-                mx = fmaxf(mx, x[i]);
+                for (int i = 0; i < 8; i++)
+                    t[i] = x[i];
+#pragma unroll
+                for (int i = 8; i < kTcKeys; i++)
+                    t[i & 7] = fmaxf(t[i & 7], x[i]);
+                mraw = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])),
+                             fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7])));
+            }
+            const float sl = p.scale_log2;
+            const float mx = mraw == -INFINITY ? -INFINITY : mraw * sl;
             if (__any_sync(FULL, mx > m + kLazy)) {
                 const float mn = fmaxf(m, mx);
                 const float alpha = mn == -INFINITY ? 1.f : fast_exp2(m - mn);
@@ -339,17 +362,24 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 l *= alpha;
                 m = mn;
             }
-            const float mu = m == -INFINITY ? 0.f : m;
+            const float nmu = m == -INFINITY ? 0.f : -m;
             {
                 uint32_t hi[32], lo[32];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int i = 0; i < 32; i++) {
-                    const float p0 = fast_exp2(x[2 * i] - mu), p1 = fast_exp2(x[2 * i + 1] - mu);
-                    l += p0 + p1;
+                    float p0 = fast_exp2(fmaf(x[2 * i], sl, nmu));
+                    float p1 = fast_exp2(fmaf(x[2 * i + 1], sl, nmu));
+                    if (masked) {  // exact zeros for masked keys (also when the scale is 0)
+                        p0 = x[2 * i] == -INFINITY ? 0.f : p0;
+                        p1 = x[2 * i + 1] == -INFINITY ? 0.f : p1;
+                    }
+                    ls[i & 3] += p0 + p1;
                     hi[i] = pack_bf16x2(p0, p1);
                     const float2 h = bf16x2_to_float2(hi[i]);
                     lo[i] = pack_bf16x2(p0 - h.x, p1 - h.y);
                 }
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 tc::st32(tS + tl, hi);
                 tc::st32(tS + tl + 32, lo);
                 tc::wait_st();
@@ -357,9 +387,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             // V rows past k_len or in unloaded boxes: zero them (all four warps)
             if (mask != 0xFu || key_base + kTcKeys > k_len) {
                 // after the V copies of this tile have landed
-                if (!(ok = __all_sync(FULL, mbar_wait(&v_full[s], (j / kTcStages) & 1))))
+                const int sv = j % kTcVStages;
+                if (!(ok = __all_sync(FULL, mbar_wait(&v_full[sv], (j / kTcVStages) & 1))))
                     break;
-                uint8_t *vt = sKV + (size_t)s * 2 * kTile + kTile;
+                uint8_t *vt = sV + (size_t)sv * kTile;
                 for (int it = r; it < HALVES * kTcKeys * 8; it += 128) {
                     const int h = it / (kTcKeys * 8), kr = (it / 8) % kTcKeys, c = it % 8;
                     if (key_base + kr >= k_len || !((mask >> (kr / kBox)) & 1u))

@@ -262,3 +262,26 @@ def test_cuda_graph_capture_and_replay(pkv):
         g.replay()
     torch.cuda.synchronize()
     compare(bits_host(out), ref, "graph replay")
+
+
+@pytest.mark.parametrize("scale", [-0.09, 0.0, 0.3])
+def test_negative_zero_and_large_scales(pkv, scale):
+    rng = np.random.default_rng(516)
+    w = _random(rng, 2, 128, 16, [1, 30, 70], [0, 16, 32])
+    w.scale = scale
+    kc, vc = stored(w)
+    ref = oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k, scale)
+    compare(bits_host(run_step(pkv, w, to_dev(w))), ref, f"scale={scale}")
+
+
+def test_repeated_full_size_runs_are_bit_identical(pkv):
+    """The kernel has no atomics or order-dependent sums across CTAs, so every
+    run of a step gives the same bits; a race between its warps would not."""
+    w = wl.prefill_config_workload(1)
+    d = to_dev(w)
+    pkv.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slots"])
+    first = bits_host(run_step(pkv, w, d, store=False))
+    out = torch.empty_like(d["q"])
+    for _ in range(12):
+        out.zero_()
+        np.testing.assert_array_equal(bits_host(run_step(pkv, w, d, out=out, store=False)), first)
