@@ -165,54 +165,77 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             for (int h = 0; h < HALVES; h++)
                 tma_load_4d(sQ + h * kQHalf, &tmq, 0, h, kvh * G, cq0 + tok0, q_full);
         }
-        // lanes 0-3 stream K boxes, lanes 4-7 V boxes, each group at its own pace
-        const int grp = lane >> 2, gl = lane & 3;
-        const unsigned gmask = 0xFu << (4 * grp);
-        uint64_t *full_bar = grp == 0 ? k_full : v_full;
-        uint64_t *empty_bar = grp == 0 ? k_empty : v_empty;
-        const CUtensorMap *map = grp == 0 ? &tmk : &tmv;
-        const int nst = grp == 0 ? kTcKStages : kTcVStages;
-        uint8_t *ring = grp == 0 ? sK : sV;
+        // One converged loop serves both rings: it probes (without blocking)
+        // whether the next K stage and the next V stage are free and issues
+        // whichever tile can go; lanes 0-3 resolve and copy one 16-token box
+        // each.  K runs ahead of V by up to its ring depth.
+        auto issue = [&](int j, bool is_k) {
+            uint64_t *fb = is_k ? k_full : v_full;
+            const int nst = is_k ? kTcKStages : kTcVStages;
+            const int s = j % nst;
+            const int key0 = j * kTcKeys + lane * kBox;
+            bool loaded = false;
+            int row = 0;
+            if (lane < kTcKeys / kBox && key0 < k_len) {
+                const int blk = __ldg(table + key0 / p.bs);
+                loaded = blk >= 0 && blk < p.NB;
+                if (!loaded && is_k)
+                    flag_error(p.err_flag, 0x2 /* PKV_FLAG_BAD_BLOCK */);
+                row = blk * p.bs + key0 % p.bs;
+            }
+            const uint32_t mask = __ballot_sync(FULL, loaded);
+            if (lane == 0)
+                mbar_arrive_expect_tx(&fb[s], (uint32_t)__popc(mask) * kBoxBytes);
+            __syncwarp();
+            if (loaded) {
+                uint8_t *dst = (is_k ? sK : sV) + (size_t)s * kTile + lane * (kBox * 128);
+                const CUtensorMap *map = is_k ? &tmk : &tmv;
+#pragma unroll
+                for (int h = 0; h < HALVES; h++)
+                    tma_load_4d(dst + h * kTileHalf, map, 0, h, kvh, row, &fb[s]);
+            }
+        };
+        int jk = 0, jv = 0;
         bool ok = true;
-        int issued = 0;
-        if (lane < 8) {
-            for (int j = 0; j < nkt; j++) {
-                const int s = j % nst;
-                if (!__all_sync(gmask, mbar_wait(&empty_bar[s], ((j / nst) & 1) ^ 1))) {
+        uint64_t t_last = global_timer_ns();
+        while (jk < nkt || jv < nkt) {
+            bool prog = false;
+            if (jk < nkt) {
+                const bool free_k = tc::test_wait(smem_u32(&k_empty[jk % kTcKStages]),
+                                                  ((jk / kTcKStages) & 1) ^ 1);
+                if (__shfl_sync(FULL, free_k, 0)) {
+                    issue(jk++, true);
+                    prog = true;
+                }
+            }
+            if (jv < jk) {
+                const bool free_v = tc::test_wait(smem_u32(&v_empty[jv % kTcVStages]),
+                                                  ((jv / kTcVStages) & 1) ^ 1);
+                if (__shfl_sync(FULL, free_v, 0)) {
+                    issue(jv++, false);
+                    prog = true;
+                }
+            }
+            if (prog) {
+                t_last = global_timer_ns();
+            } else {
+                __nanosleep(32);
+                if (__shfl_sync(FULL, global_timer_ns() - t_last > 2000000000ull, 0)) {
                     ok = false;
                     break;
                 }
-                const int key0 = j * kTcKeys + gl * kBox;
-                bool loaded = false;
-                int row = 0;
-                if (key0 < k_len) {
-                    const int blk = __ldg(table + key0 / p.bs);
-                    loaded = blk >= 0 && blk < p.NB;
-                    if (!loaded && grp == 0)
-                        flag_error(p.err_flag, 0x2 /* PKV_FLAG_BAD_BLOCK */);
-                    row = blk * p.bs + key0 % p.bs;
-                }
-                const uint32_t mask = (__ballot_sync(gmask, loaded) >> (4 * grp)) & 0xFu;
-                if (gl == 0)
-                    mbar_arrive_expect_tx(&full_bar[s], (uint32_t)__popc(mask) * kBoxBytes);
-                __syncwarp(gmask);
-                if (loaded) {
-                    uint8_t *dst = ring + (size_t)s * kTile + gl * (kBox * 128);
-#pragma unroll
-                    for (int h = 0; h < HALVES; h++)
-                        tma_load_4d(dst + h * kTileHalf, map, 0, h, kvh, row, &full_bar[s]);
-                }
-                issued = j + 1;
             }
-            if (!ok && gl == 0)
+        }
+        if (lane == 0) {
+            if (!ok)
                 flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
             // copies still in flight land before the CTA may exit
-            if (gl == 0)
-                for (int j = max(0, issued - nst); j < issued; j++)
-                    mbar_wait(&full_bar[j % nst], (j / nst) & 1);
-        }
-        if (lane == 0)
             mbar_wait(q_full, 0);
+            for (int j = max(0, jk - kTcKStages); j < jk; j++)
+                mbar_wait(&k_full[j % kTcKStages], (j / kTcKStages) & 1);
+            for (int j = max(0, jv - kTcVStages); j < jv; j++)
+                mbar_wait(&v_full[j % kTcVStages], (j / kTcVStages) & 1);
+        }
         __syncwarp();
     } else if (warp == 5) {
         // ----------------------------------------------------------------- MMA
@@ -245,8 +268,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     // S_{j+1} overwrites the buffer P_{j-1} occupies: the tensor pipe
                     // does not order P.V_{j-1}'s TMEM reads before a later MMA's
                     // writes, so wait for P.V_{j-1} (long done, a softmax ago)
-                    if (j >= 1 && !(ok = mbar_wait(o_done, (j - 1) & 1)))
-                        break;
+                    if (j >= 1) {
+                        if (!(ok = mbar_wait(o_done, (j - 1) & 1)))
+                            break;
+                        tc::fence_after();
+                    }
                     issue_s(j + 1);
                 }
                 if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1)))
@@ -268,7 +294,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
             if (!ok)
                 flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
-            // every MMA issued has completed before TMEM is released
+            // every MMA issued has completed before TMEM is released (and
+            // before the softmax warps read O)
             tc::commit(smem_u32(mma_done));
             mbar_wait(mma_done, 0);
         }
@@ -404,8 +431,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             if (lane == 0)
                 mbar_arrive(&p_full[j & 1]);
         }
+        // all P.V done: mma_done completes exactly once (o_done's parity is
+        // ambiguous here, since P.V_{nkt-2} may still be running)
         if (ok)
-            ok = __all_sync(FULL, mbar_wait(o_done, (nkt - 1) & 1));
+            ok = __all_sync(FULL, mbar_wait(mma_done, 0));
         if (!ok) {
             if (lane == 0)
                 flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);

@@ -78,6 +78,17 @@ __device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols)
                  : "memory");
 }
 
+// Non-blocking probe of an mbarrier phase (never suspends the thread).
+__device__ __forceinline__ bool test_wait(uint32_t mbar_saddr, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(mbar_saddr), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
