@@ -25,6 +25,7 @@
 namespace pkv {
 
 constexpr int kMergeWarps = 4;
+constexpr int kFastPieces = 8;  // rows with at most this many pieces load everything at once
 
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_pieces_kernel(const DecodeParams p)
@@ -69,6 +70,49 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_pieces_kernel(const De
         return p.ws_part + (((size_t)w * 2 + slot) * G + g) * (D + 4);
     };
 
+    using Vec = typename std::conditional<DPL == 4, float4, float2>::type;
+    if (n <= kFastPieces) {
+        // Few pieces (the common case): every load of the row in flight at once.
+        Vec x[kFastPieces];
+        float mi[kFastPieces], li[kFastPieces];
+#pragma unroll
+        for (int i = 0; i < kFastPieces; i++) {
+            if (i < n) {
+                const float *pc = piece(i);
+                x[i] = *reinterpret_cast<const Vec *>(pc + lane * DPL);
+                mi[i] = pc[D];
+                li[i] = pc[D + 1];
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kFastPieces; i++)
+            if (i < n)
+                M = fmaxf(M, mi[i]);
+        float acc[DPL], Ls = 0.f;
+#pragma unroll
+        for (int c = 0; c < DPL; c++)
+            acc[c] = 0.f;
+        if (M != -INFINITY) {  // else no token of the stream could be read: zeros
+#pragma unroll
+            for (int i = 0; i < kFastPieces; i++) {
+                if (i < n) {
+                    const float w = fast_exp2(mi[i] - M);
+                    Ls += li[i] * w;
+                    const float *xv = reinterpret_cast<const float *>(&x[i]);
+#pragma unroll
+                    for (int c = 0; c < DPL; c++)
+                        acc[c] += w * xv[c];
+                }
+            }
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+        for (int c = 0; c < DPL; c++)
+            o[c] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[c] * inv));
+        return;
+    }
+
     float M = -INFINITY;
     for (int i = lane; i < n; i += 32)
         M = fmaxf(M, piece(i)[D]);
@@ -89,7 +133,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_pieces_kernel(const De
         Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
 
     // Weighted sum of the partial outputs; 8 pieces' loads in flight at once.
-    using Vec = typename std::conditional<DPL == 4, float4, float2>::type;
     float acc[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; i++)
