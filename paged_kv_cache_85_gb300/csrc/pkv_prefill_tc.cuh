@@ -67,6 +67,130 @@ __host__ __device__ inline TcSmem tc_smem_layout(int D)
     return L;
 }
 
+__device__ __forceinline__ bool prefill_seq_sane(const PrefillParams &p, int cq0, int cq1, int ck0,
+                                                 int ck1)
+{
+    const int q_len = cq1 - cq0, k_len = ck1 - ck0;
+    return cq0 >= 0 && q_len >= 0 && (long long)cq1 <= p.Tq && k_len >= q_len &&
+           k_len <= p.MBS * p.bs && q_len <= p.max_q;
+}
+
+// Query tiles of one sequence whose causal key range spans at least c key
+// tiles.  A tile's range grows with its index, so these are its last tiles.
+template <int TPC>
+__device__ __forceinline__ int tiles_at_least(int q_len, int base, int c)
+{
+    if (q_len <= 0)
+        return 0;
+    const int nt = (q_len + TPC - 1) / TPC;
+    // tile t reaches key tile c-1 iff min(q_len, (t+1) TPC) >= need
+    const int need = kTcKeys * (c - 1) - base + 1;
+    if (need <= 0)
+        return nt;
+    if (need > q_len)
+        return 0;
+    return nt - ((need + TPC - 1) / TPC - 1);
+}
+
+struct PrefillWork {
+    int b, kvh, tile;  // b < 0: nothing to do
+};
+constexpr int kSchedChunks = 8;  // sequences per lane in the longest-first schedule
+constexpr int kSchedMaxSeqs = 32 * kSchedChunks;
+
+// The (sequence, KV head, query tile) this CTA works on, run by one warp.
+// CTAs start in launch order, so the work is handed out longest first (a
+// tile's cost is its number of key tiles): with up to kSchedMaxSeqs
+// sequences the CTA's rank r (its launch index over the KV heads) is mapped
+// to the r-th tile in decreasing cost, found by a binary search over the
+// cost with per-sequence closed-form counts.  Beyond that many sequences the
+// last tile of every sequence goes first, then the second-to-last ones, and
+// so on.
+template <int TPC>
+__device__ PrefillWork prefill_schedule(const PrefillParams &p, int lane)
+{
+    constexpr unsigned FULL = 0xffffffffu;
+    const int B = (int)gridDim.z, Hkv = (int)gridDim.y, X = (int)gridDim.x;
+    const unsigned lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const int r = (int)(lin / (unsigned)Hkv);
+    PrefillWork w{-1, (int)(lin % (unsigned)Hkv), 0};
+    if (B > kSchedMaxSeqs) {
+        w.b = r % B;
+        w.tile = X - 1 - r / B;
+        return w;
+    }
+    int qv[kSchedChunks], bv[kSchedChunks];
+    int cmax = 1;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kSchedChunks; i++) {
+        const int s = lane + 32 * i;
+        qv[i] = 0;
+        bv[i] = 0;
+        if (s < B) {
+            const int cq0 = __ldg(p.cu_q + s), cq1 = __ldg(p.cu_q + s + 1);
+            const int ck0 = __ldg(p.cu_k + s), ck1 = __ldg(p.cu_k + s + 1);
+            if (prefill_seq_sane(p, cq0, cq1, ck0, ck1)) {
+                qv[i] = cq1 - cq0;
+                bv[i] = (ck1 - ck0) - (cq1 - cq0);
+                if (ck1 > ck0)
+                    cmax = max(cmax, (ck1 - ck0 - 1) / kTcKeys + 1);
+            } else {
+                bad = true;
+            }
+        }
+    }
+    // sequences with bad lengths get no work; one CTA reports them
+    if (bad && lin == 0)
+        flag_error(p.err_flag, 0x4 /* PKV_FLAG_BAD_CONTEXT_LEN */);
+    cmax = __reduce_max_sync(FULL, cmax);
+    auto count = [&](int c) {
+        int n = 0;
+#pragma unroll
+        for (int i = 0; i < kSchedChunks; i++)
+            n += tiles_at_least<TPC>(qv[i], bv[i], c);
+        return (int)__reduce_add_sync(FULL, (unsigned)n);
+    };
+    if (r >= count(1))
+        return w;
+    int lo = 1, hi = cmax + 1;  // count(lo) > r >= count(hi)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (count(mid) > r)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    // rank among the tiles costing exactly lo, in sequence order
+    const int rp = r - count(lo + 1);
+    int acc = 0;
+#pragma unroll
+    for (int i = 0; i < kSchedChunks; i++) {
+        const int at = tiles_at_least<TPC>(qv[i], bv[i], lo);
+        const int n = at - tiles_at_least<TPC>(qv[i], bv[i], lo + 1);
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(FULL, incl, off);
+            if (lane >= off)
+                incl += y;
+        }
+        const int total = __shfl_sync(FULL, incl, 31);
+        if (rp < acc + total) {
+            const int ex = acc + incl - n;
+            const bool mine = rp >= ex && rp < ex + n;
+            const int src = __ffs(__ballot_sync(FULL, mine)) - 1;
+            const int nt = (qv[i] + TPC - 1) / TPC;
+            const int t = nt - at + (rp - ex);  // the first tile costing lo, plus the rank
+            w.b = src + 32 * i;
+            w.tile = __shfl_sync(FULL, t, src);
+            return w;
+        }
+        acc += total;
+    }
+    return w;  // not reached: rp < count(lo) - count(lo + 1)
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kTcThreads, 2)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq,
@@ -101,17 +225,26 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     uint8_t *sV = sK + (size_t)kTcKStages * (D / 64) * kTcKeys * 128;  // kTcVStages V tiles
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.z, kvh = blockIdx.y;
-    const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;  // the longest tiles start first
 
     grid_launch_dependents();
+    __shared__ int s_work[3];
+    if (warp == 0) {
+        const PrefillWork w = prefill_schedule<TPC>(p, lane);
+        if (lane == 0) {
+            s_work[0] = w.b;
+            s_work[1] = w.kvh;
+            s_work[2] = w.tile;
+        }
+    }
+    __syncthreads();
+    const int b = s_work[0], kvh = s_work[1], tile = s_work[2];
+    if (b < 0)
+        return;
     const int cq0 = __ldg(p.cu_q + b), cq1 = __ldg(p.cu_q + b + 1);
     const int ck0 = __ldg(p.cu_k + b), ck1 = __ldg(p.cu_k + b + 1);
     const int q_len = cq1 - cq0, k_len = ck1 - ck0;
-    const bool sane = cq0 >= 0 && q_len >= 0 && (long long)cq1 <= p.Tq && k_len >= q_len &&
-                      k_len <= p.MBS * p.bs && q_len <= p.max_q;
-    if (!sane) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0)
+    if (!prefill_seq_sane(p, cq0, cq1, ck0, ck1)) {
+        if (threadIdx.x == 0)
             flag_error(p.err_flag, 0x4 /* PKV_FLAG_BAD_CONTEXT_LEN */);
         return;
     }

@@ -153,6 +153,21 @@ def test_group_dim_block_variants(pkv, G, D, bs):
     compare(bits_host(run_step(pkv, w, to_dev(w))), ref, f"G={G} D={D} bs={bs}")
 
 
+@pytest.mark.parametrize("n_seqs", [256, 300])
+def test_many_sequences_every_tile_once(pkv, n_seqs):
+    """Up to 256 sequences the CTAs take tiles longest first (ranked in the
+    kernel); beyond that the launch order is used.  Both must cover every
+    (sequence, head, tile) exactly once."""
+    rng = np.random.default_rng(520 + n_seqs)
+    q_lens = [int(x) for x in rng.integers(1, 90, size=n_seqs)]
+    cached = [16 * int(c) for c in rng.integers(0, 5, size=n_seqs)]
+    w = _random(rng, 2, 64, 16, q_lens, cached)
+    kc, vc = stored(w)
+    ref = oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k,
+                               w.scale)
+    compare(bits_host(run_step(pkv, w, to_dev(w))), ref, f"{n_seqs} sequences")
+
+
 def test_long_context_rows_across_many_tiles(pkv):
     """One long sequence (cached 1024 + 700 new) at G = 2: many K tiles and query tiles."""
     rng = np.random.default_rng(510)
