@@ -186,7 +186,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
     if (start < end)
         locate_box(start, pb, p.B, cb, ch, cj);
     int lb = cb, lh = ch, lj = cj, lpos = start;  // look-ahead cursor
-    int qb[kLookahead];                          // block ids of boxes pos .. pos + kLookahead - 1
+    int qb[kLookahead];  // qb[(pos - start) % kLookahead]: block id of box pos, loaded ahead
 #pragma unroll
     for (int i = 0; i < kLookahead; i++) {
         qb[i] = -1;
@@ -203,10 +203,18 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
 
     int stage = 0;
     uint32_t phase = 0;
-    for (;;) {
+    bool more = true;
+    while (more) {
+    // Unrolled by the queue depth: round u uses and refills qb[u] in place,
+    // so a block id is first read kLookahead rounds after its load was issued
+    // (a shifting queue would wait on the newest load every round).
+#pragma unroll
+    for (int u = 0; u < kLookahead; u++) {
         const bool mine = pos < end;
-        if (!__any_sync(FULL, mine))
+        if (!__any_sync(FULL, mine)) {
+            more = false;
             break;
+        }
         if (!__all_sync(FULL, mbar_wait(&empty[stage], phase ^ 1))) {
             if (lane == 0)
                 flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
@@ -216,7 +224,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
         int flags = 0, row = 0, b = cb, h = ch;
         if (mine) {
             const int j = cj;
-            const int blk = qb[0];
+            const int blk = qb[u];
             const int nb = pb[b + 1] - pb[b];
             const int tok0 = j * kBox;
             const bool loaded = blk >= 0 && blk < p.NB;
@@ -241,12 +249,9 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
             // advance both cursors
             next_box(pb, p.B, cb, ch, cj);
             ++pos;
-#pragma unroll
-            for (int i = 0; i + 1 < kLookahead; i++)
-                qb[i] = qb[i + 1];
-            qb[kLookahead - 1] = -1;
+            qb[u] = -1;
             if (lpos < end) {
-                qb[kLookahead - 1] = box_block(p, lb, lj);
+                qb[u] = box_block(p, lb, lj);
                 next_box(pb, p.B, lb, lh, lj);
             }
             ++lpos;
@@ -278,6 +283,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
             stage = 0;
             phase ^= 1;
         }
+    }
     }
     // Tell the consumers there is no more work.
     if (!__all_sync(FULL, mbar_wait(&empty[stage], phase ^ 1))) {
