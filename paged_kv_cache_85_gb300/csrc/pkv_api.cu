@@ -326,15 +326,17 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
     if (box_max >= 0x7fffffffLL)
         return fail(PKV_ERR_UNSUPPORTED, "paged_attn_decode: B*Hkv*MBS*bs/16 must be < 2^31");
     // Prefer 4-worker CTAs, three per SM for FP8 caches (their kernels are
-    // built for three) and two for bf16; fall back to one 8-worker CTA per
-    // SM when they do not fit (large B, or G = 8 with D = 128).
+    // built for three; up to four stages where they fit, since the FP8 path
+    // is bound by the bytes its copies keep in flight) and two for bf16; fall
+    // back to one 8-worker CTA per SM when they do not fit (large B, or G = 8
+    // with D = 128).
     const size_t pair_smem = pkv::kSmemPerSm / 2 - pkv::kSmemReserve;
     const size_t trio_smem = pkv::kSmemPerSm / 3 - pkv::kSmemReserve;
     const int eb = f8 ? 1 : 2;  // bytes per cached element
     int NW = pkv::kPairWorkers;
     int stages = 0;
     if (f8)
-        stages = pkv::decode_stages_for(D, G, NW, B, pkv::kPairStages, trio_smem, eb);
+        stages = pkv::decode_stages_for(D, G, NW, B, pkv::kMaxStages, trio_smem, eb);
     if (stages < pkv::kPairStages)
         stages = pkv::decode_stages_for(D, G, NW, B, pkv::kPairStages, pair_smem, eb);
     if (stages < pkv::kPairStages) {
