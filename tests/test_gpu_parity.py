@@ -241,6 +241,52 @@ def test_error_flags_and_skips(pkv):
     assert int(err.item()) & pkv.FLAG_BAD_CONTEXT_LEN
 
 
+def test_empty_batch_is_a_no_op(pkv):
+    """B = 0 decode and N = 0 store succeed and touch nothing; a store whose
+    slots are all padding (-1) leaves the cache bit-identical."""
+    rng = np.random.default_rng(13)
+    w = _random_problem(rng, 3, 4, 2, 64, 16, [5, 40, 300])
+    d = to_dev(w)
+    kc0, vc0 = bits_host(d["k_cache"]).copy(), bits_host(d["v_cache"]).copy()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.store_kvcache(d["k_new"][:0], d["v_new"][:0], d["k_cache"], d["v_cache"], d["slots"][:0],
+                      err_flag=err)
+    q0 = d["q"][:0]
+    out0 = torch.empty_like(q0)
+    pkv.paged_attn_decode(q0, d["k_cache"], d["v_cache"], d["tables"][:0], d["lens"][:0], w.scale,
+                          out0, err_flag=err)
+    pad = torch.full_like(d["slots"], -1)
+    pkv.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], pad, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(bits_host(d["k_cache"]), kc0)
+    np.testing.assert_array_equal(bits_host(d["v_cache"]), vc0)
+
+
+def test_maximum_batch_parity_and_one_past_it_is_rejected(pkv):
+    """8192 sequences (the most one call takes: their box prefix sums live in
+    shared memory) match the oracle; 8193 are refused before any launch."""
+    rng = np.random.default_rng(14)
+    B = 8192
+    lens = rng.integers(1, 41, size=B)
+    w = _random_problem(rng, B, 2, 1, 64, 16, lens)
+    kc, vc, ref = oracle_step(w)
+    d = to_dev(w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_step(pkv, w, d, err=err)
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(bits_host(d["k_cache"]), kc)
+    compare(out, ref, "B=8192")
+    q1 = torch.zeros((B + 1, 2, 64), dtype=torch.bfloat16, device="cuda")
+    tables1 = torch.zeros((B + 1, d["tables"].shape[1]), dtype=torch.int32, device="cuda")
+    lens1 = torch.ones(B + 1, dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_attn_decode(q1, d["k_cache"], d["v_cache"], tables1, lens1, w.scale,
+                              torch.empty_like(q1), workspace=torch.zeros(16, dtype=torch.uint8,
+                                                                            device="cuda"))
+    assert e.value.status == 2  # PKV_ERR_UNSUPPORTED
+
+
 def test_workspace_too_small_is_rejected(pkv):
     w, _ = config(0)
     d = to_dev(w)
