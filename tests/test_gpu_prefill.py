@@ -78,9 +78,9 @@ def compare(got, ref, what=""):
 
 def sample_pairs(w, rng, per_seq=48):
     """(row, head) pairs: every sequence's first and last tokens, tokens on
-    both sides of the kernel's 112-row tile boundaries, and random tokens;
-    random heads."""
-    tpc = 112 // w.G
+    both sides of the kernel's query-tile boundaries (128 (token, head) rows,
+    so 128 / G tokens per tile), and random tokens; random heads."""
+    tpc = 128 // w.G
     rows = []
     for b in range(w.B):
         ql = int(w.q_lens[b])
