@@ -93,8 +93,10 @@ __device__ __forceinline__ int tiles_at_least(int q_len, int base, int c)
 }
 
 struct PrefillWork {
-    int b, kvh, tile;  // b < 0: nothing to do
+    int b, kvh, tile;        // b < 0: nothing to do
+    int cq0, cq1, ck0, ck1;  // sequence b's boundaries (cq0 == kNotLoaded: read them again)
 };
+constexpr int kNotLoaded = -2147483647 - 1;
 constexpr int kSchedChunks = 8;  // sequences per lane in the longest-first schedule
 constexpr int kSchedMaxSeqs = 32 * kSchedChunks;
 
@@ -105,31 +107,35 @@ constexpr int kSchedMaxSeqs = 32 * kSchedChunks;
 // to the r-th tile in decreasing cost, found by a binary search over the
 // cost with per-sequence closed-form counts.  Beyond that many sequences the
 // last tile of every sequence goes first, then the second-to-last ones, and
-// so on.
-template <int TPC>
+// so on.  NCH chunks of 32 sequences are scanned (one lane per sequence).
+template <int TPC, int NCH>
 __device__ PrefillWork prefill_schedule(const PrefillParams &p, int lane)
 {
     constexpr unsigned FULL = 0xffffffffu;
     const int B = (int)gridDim.z, Hkv = (int)gridDim.y, X = (int)gridDim.x;
     const unsigned lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
     const int r = (int)(lin / (unsigned)Hkv);
-    PrefillWork w{-1, (int)(lin % (unsigned)Hkv), 0};
+    PrefillWork w{-1, (int)(lin % (unsigned)Hkv), 0, kNotLoaded, 0, 0, 0};
     if (B > kSchedMaxSeqs) {
         w.b = r % B;
         w.tile = X - 1 - r / B;
         return w;
     }
-    int qv[kSchedChunks], bv[kSchedChunks];
+    int qv[NCH], bv[NCH], q0v[NCH], k0v[NCH];
     int cmax = 1;
     bool bad = false;
 #pragma unroll
-    for (int i = 0; i < kSchedChunks; i++) {
+    for (int i = 0; i < NCH; i++) {
         const int s = lane + 32 * i;
         qv[i] = 0;
         bv[i] = 0;
+        q0v[i] = 0;
+        k0v[i] = 0;
         if (s < B) {
             const int cq0 = __ldg(p.cu_q + s), cq1 = __ldg(p.cu_q + s + 1);
             const int ck0 = __ldg(p.cu_k + s), ck1 = __ldg(p.cu_k + s + 1);
+            q0v[i] = cq0;
+            k0v[i] = ck0;
             if (prefill_seq_sane(p, cq0, cq1, ck0, ck1)) {
                 qv[i] = cq1 - cq0;
                 bv[i] = (ck1 - ck0) - (cq1 - cq0);
@@ -147,7 +153,7 @@ __device__ PrefillWork prefill_schedule(const PrefillParams &p, int lane)
     auto count = [&](int c) {
         int n = 0;
 #pragma unroll
-        for (int i = 0; i < kSchedChunks; i++)
+        for (int i = 0; i < NCH; i++)
             n += tiles_at_least<TPC>(qv[i], bv[i], c);
         return (int)__reduce_add_sync(FULL, (unsigned)n);
     };
@@ -165,7 +171,7 @@ __device__ PrefillWork prefill_schedule(const PrefillParams &p, int lane)
     const int rp = r - count(lo + 1);
     int acc = 0;
 #pragma unroll
-    for (int i = 0; i < kSchedChunks; i++) {
+    for (int i = 0; i < NCH; i++) {
         const int at = tiles_at_least<TPC>(qv[i], bv[i], lo);
         const int n = at - tiles_at_least<TPC>(qv[i], bv[i], lo + 1);
         int incl = n;
@@ -184,6 +190,11 @@ __device__ PrefillWork prefill_schedule(const PrefillParams &p, int lane)
             const int t = nt - at + (rp - ex);  // the first tile costing lo, plus the rank
             w.b = src + 32 * i;
             w.tile = __shfl_sync(FULL, t, src);
+            // the winner lane's sequence passed on, so it is not read again
+            w.cq0 = __shfl_sync(FULL, q0v[i], src);
+            w.ck0 = __shfl_sync(FULL, k0v[i], src);
+            w.cq1 = w.cq0 + __shfl_sync(FULL, qv[i], src);
+            w.ck1 = w.ck0 + __shfl_sync(FULL, qv[i] + bv[i], src);
             return w;
         }
         acc += total;
@@ -227,35 +238,23 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     grid_launch_dependents();
-    __shared__ int s_work[3];
+    // Prologue, in parallel: warp 0 finds this CTA's work, the producer warp
+    // initialises the barriers, the MMA warp allocates TMEM; one barrier then
+    // publishes all three.
+    __shared__ int s_work[7];
     if (warp == 0) {
-        const PrefillWork w = prefill_schedule<TPC>(p, lane);
+        const PrefillWork w = gridDim.z <= 32 ? prefill_schedule<TPC, 1>(p, lane)
+                                              : prefill_schedule<TPC, kSchedChunks>(p, lane);
         if (lane == 0) {
             s_work[0] = w.b;
             s_work[1] = w.kvh;
             s_work[2] = w.tile;
+            s_work[3] = w.cq0;
+            s_work[4] = w.cq1;
+            s_work[5] = w.ck0;
+            s_work[6] = w.ck1;
         }
-    }
-    __syncthreads();
-    const int b = s_work[0], kvh = s_work[1], tile = s_work[2];
-    if (b < 0)
-        return;
-    const int cq0 = __ldg(p.cu_q + b), cq1 = __ldg(p.cu_q + b + 1);
-    const int ck0 = __ldg(p.cu_k + b), ck1 = __ldg(p.cu_k + b + 1);
-    const int q_len = cq1 - cq0, k_len = ck1 - ck0;
-    if (!prefill_seq_sane(p, cq0, cq1, ck0, ck1)) {
-        if (threadIdx.x == 0)
-            flag_error(p.err_flag, 0x4 /* PKV_FLAG_BAD_CONTEXT_LEN */);
-        return;
-    }
-    const int tok0 = tile * TPC;
-    if (tok0 >= q_len)
-        return;
-    const int base = k_len - q_len;  // position of new token 0
-    const int last_pos = base + min(q_len, tok0 + TPC) - 1;
-    const int nkt = last_pos / kTcKeys + 1;
-
-    if (threadIdx.x == 0) {
+    } else if (warp == 4 && lane == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < kTcKStages; s++) {
             mbar_init(&k_full[s], 1);
@@ -272,8 +271,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         mbar_init(o_done, 1);
         mbar_init(mma_done, 1);
         fence_mbarrier_init();
-    }
-    if (warp == 5) {
+    } else if (warp == 5) {
         tc::alloc(smem_u32(slot), kTcCols);
         tc::relinquish();
     }
@@ -281,6 +279,28 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *slot;
+    const int b = s_work[0], kvh = s_work[1], tile = s_work[2];
+    int cq0 = s_work[3], cq1 = s_work[4], ck0 = s_work[5], ck1 = s_work[6];
+    if (b >= 0 && cq0 == kNotLoaded) {
+        cq0 = __ldg(p.cu_q + b);
+        cq1 = __ldg(p.cu_q + b + 1);
+        ck0 = __ldg(p.cu_k + b);
+        ck1 = __ldg(p.cu_k + b + 1);
+    }
+    const int q_len = cq1 - cq0, k_len = ck1 - ck0;
+    const int tok0 = tile * TPC;
+    const bool sane = b >= 0 && prefill_seq_sane(p, cq0, cq1, ck0, ck1);
+    if (!sane || tok0 >= q_len) {
+        // nothing to do (or a bad sequence): release TMEM and leave
+        if (b >= 0 && !sane && threadIdx.x == 0)
+            flag_error(p.err_flag, 0x4 /* PKV_FLAG_BAD_CONTEXT_LEN */);
+        if (warp == 5)
+            tc::dealloc(tmem, kTcCols);
+        return;
+    }
+    const int base = k_len - q_len;  // position of new token 0
+    const int last_pos = base + min(q_len, tok0 + TPC) - 1;
+    const int nkt = last_pos / kTcKeys + 1;
     const uint32_t tO = tmem, tS0 = tmem + kTcSCol;
 
     if (warp == 4) {
