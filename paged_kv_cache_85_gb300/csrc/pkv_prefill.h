@@ -18,7 +18,9 @@ struct PrefillParams {
     int32_t *err_flag;            // nullable
     long long Tq;
     int B, Hq, Hkv, MBS, bs, NB;
-    int max_q;                    // the caller's bound on q_len (sizes the grid)
+    int max_q;                    // the caller's bound on q_len (sizes the work space)
+    int X;                        // query tiles per sequence at max_q
+    int n_items;                  // work items: X tiles x Hkv heads x B sequences
     float scale_log2;             // |scale| * log2(e)
     int neg_scale;                // scale < 0: the score MMA negates Q
 };
