@@ -452,8 +452,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         __syncwarp();
     } else if (warp == 5) {
         // ----------------------------------------------------------------- MMA
-        if (lane == 0) {
+        // The whole warp runs the loop and waits on the barriers; one elected
+        // lane issues the MMAs and their commits (issue from a converged warp
+        // costs fewer cycles per MMA than from a lone lane).
+        {
             bool ok = true;
+            auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+                return __all_sync(FULL, mbar_wait(bar, parity));
+            };
             const uint32_t qa = smem_u32(sQ);
             // a negative scale is applied by negating Q (bit 13 of the descriptor)
             const uint32_t idS = tc::idesc_bf16(kTcRows, kTcKeys, false) | (p.neg_scale ? 1u << 13 : 0u);
@@ -465,36 +471,39 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             // (P.V_g cannot complete before S_g), so its parity wait is exact.
             auto issue_s = [&](int g, bool last_of_item) -> bool {
                 const int s = g % kTcKStages;
-                if (!mbar_wait(&k_full[s], (g / kTcKStages) & 1))
+                if (!wait_all(&k_full[s], (g / kTcKStages) & 1))
                     return false;
                 if (g >= 2) {
-                    if (!mbar_wait(&pv_done[g & 1], ((g - 2) >> 1) & 1))
+                    if (!wait_all(&pv_done[g & 1], ((g - 2) >> 1) & 1))
                         return false;
                     tc::fence_after();
                 }
                 const uint32_t ka = smem_u32(sK + (size_t)s * kTile);
                 const uint32_t dst = tS0 + (uint32_t)(g & 1) * kTcKeys;
+                if (tc::elect_one()) {
 #pragma unroll
-                for (int kq = 0; kq < D / 16; kq++) {
-                    const uint32_t off = (uint32_t)(kq >> 2) * kQHalf + (uint32_t)(kq & 3) * 32;
-                    const uint32_t offk = (uint32_t)(kq >> 2) * kTileHalf + (uint32_t)(kq & 3) * 32;
-                    tc::mma_ss(dst, tc::smem_desc(qa + off, 16, 1024),
-                               tc::smem_desc(ka + offk, 16, 1024), idS, kq > 0);
+                    for (int kq = 0; kq < D / 16; kq++) {
+                        const uint32_t off = (uint32_t)(kq >> 2) * kQHalf + (uint32_t)(kq & 3) * 32;
+                        const uint32_t offk = (uint32_t)(kq >> 2) * kTileHalf + (uint32_t)(kq & 3) * 32;
+                        tc::mma_ss(dst, tc::smem_desc(qa + off, 16, 1024),
+                                   tc::smem_desc(ka + offk, 16, 1024), idS, kq > 0);
+                    }
+                    tc::commit(smem_u32(&s_full[g & 1]));
+                    tc::commit(smem_u32(&k_empty[s]));
+                    if (last_of_item)
+                        tc::commit(smem_u32(q_empty));
                 }
-                tc::commit(smem_u32(&s_full[g & 1]));
-                tc::commit(smem_u32(&k_empty[s]));
-                if (last_of_item)
-                    tc::commit(smem_u32(q_empty));
+                __syncwarp();
                 return true;
             };
             int g0 = 0;  // tiles of the previous items
             for (int n = 0; ok; n++) {
-                if (!(ok = mbar_wait(&item_ready[n & 1], (n >> 1) & 1)))
+                if (!(ok = wait_all(&item_ready[n & 1], (n >> 1) & 1)))
                     break;
                 const PrefillItem it = items[n & 1];
                 if (it.b < 0)
                     break;
-                if (!(ok = mbar_wait(q_full, n & 1)))
+                if (!(ok = wait_all(q_full, n & 1)))
                     break;
                 tc::fence_after();
                 if (!(ok = issue_s(g0, it.nkt == 1)))
@@ -503,36 +512,42 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     const int g = g0 + j;
                     if (j + 1 < it.nkt && !(ok = issue_s(g + 1, j + 2 == it.nkt)))
                         break;
-                    if (!(ok = mbar_wait(&p_full[g & 1], (g >> 1) & 1)))
+                    if (!(ok = wait_all(&p_full[g & 1], (g >> 1) & 1)))
                         break;
-                    if (!(ok = mbar_wait(&v_full[g % kTcVStages], (g / kTcVStages) & 1)))
+                    if (!(ok = wait_all(&v_full[g % kTcVStages], (g / kTcVStages) & 1)))
                         break;
                     // the first P.V of an item overwrites O: the previous item's
                     // epilogue must have read it out
-                    if (j == 0 && n >= 1 && !(ok = mbar_wait(o_free, (n - 1) & 1)))
+                    if (j == 0 && n >= 1 && !(ok = wait_all(o_free, (n - 1) & 1)))
                         break;
                     tc::fence_after();
                     const int s = g % kTcVStages;
                     const uint32_t va = smem_u32(sV + (size_t)s * kTile);
                     const uint32_t pS = tS0 + (uint32_t)(g & 1) * kTcKeys;
+                    if (tc::elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < kTcKeys / 16; kk++) {
-                        const uint64_t dv = tc::smem_desc(va + kk * 16 * 128, kTileHalf, 1024);
-                        tc::mma_ts(tO, pS + 8 * kk, dv, idO, (j > 0 || kk > 0) ? 1u : 0u);
-                        tc::mma_ts(tO, pS + 32 + 8 * kk, dv, idO, 1u);
+                        for (int kk = 0; kk < kTcKeys / 16; kk++) {
+                            const uint64_t dv = tc::smem_desc(va + kk * 16 * 128, kTileHalf, 1024);
+                            tc::mma_ts(tO, pS + 8 * kk, dv, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                            tc::mma_ts(tO, pS + 32 + 8 * kk, dv, idO, 1u);
+                        }
+                        tc::commit(smem_u32(&v_empty[s]));
+                        tc::commit(smem_u32(&pv_done[g & 1]));
                     }
-                    tc::commit(smem_u32(&v_empty[s]));
-                    tc::commit(smem_u32(&pv_done[g & 1]));
+                    __syncwarp();
                 }
                 if (!ok)
                     break;
                 g0 += it.nkt;
-                mbar_arrive(&item_free[n & 1]);
+                if (lane == 0)
+                    mbar_arrive(&item_free[n & 1]);
             }
-            if (!ok)
+            if (!ok && lane == 0)
                 flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
             // every MMA issued has completed before TMEM is released
-            tc::commit(smem_u32(mma_done));
+            if (tc::elect_one())
+                tc::commit(smem_u32(mma_done));
+            __syncwarp();
             mbar_wait(mma_done, 0);
         }
         __syncwarp();

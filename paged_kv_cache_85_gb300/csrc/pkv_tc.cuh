@@ -122,5 +122,14 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32])
         : "memory");
 }
 
+// True in one lane of the (converged) warp, the same lane on every call.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(pred));
+    return pred != 0;
+}
+
 } // namespace tc
 } // namespace pkv
