@@ -168,6 +168,26 @@ def test_many_sequences_every_tile_once(pkv, n_seqs):
     compare(bits_host(run_step(pkv, w, to_dev(w))), ref, f"{n_seqs} sequences")
 
 
+@pytest.mark.parametrize("n_seqs", [5, 300])
+def test_loose_max_seqlen_q_gives_the_same_bits(pkv, n_seqs):
+    """max_seqlen_q only bounds the work space: a bound far above every query
+    length leaves most work positions empty, and the persistent CTAs must
+    skip or stop at them and still produce every row, bit for bit."""
+    rng = np.random.default_rng(530 + n_seqs)
+    q_lens = [int(x) for x in rng.integers(1, 70, size=n_seqs)]
+    cached = [16 * int(c) for c in rng.integers(0, 4, size=n_seqs)]
+    w = _random(rng, 2, 64, 16, q_lens, cached)
+    d = to_dev(w)
+    tight = bits_host(run_step(pkv, w, d))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(d["q"])
+    pkv.paged_prefill(d["q"], d["k_cache"], d["v_cache"], d["tables"], d["cu_q"], d["cu_k"],
+                      8 * w.max_seqlen_q, w.scale, out, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(bits_host(out), tight)
+
+
 def test_long_context_rows_across_many_tiles(pkv):
     """One long sequence (cached 1024 + 700 new) at G = 2: many K tiles and query tiles."""
     rng = np.random.default_rng(510)
