@@ -177,7 +177,8 @@ pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void 
  *   block_tables  device, int32 [B, MBS]; entries past ceil(k_len / bs) unread
  *   cu_seqlens_q  device, int32 [B + 1], non-decreasing, cu_seqlens_q[B] <= Tq
  *   cu_seqlens_k  device, int32 [B + 1]; q_len <= k_len <= MBS * bs
- *   max_seqlen_q  host bound on every q_len (sizes the grid)
+ *   max_seqlen_q  host bound on every q_len (sizes the work space; a loose
+ *                 bound only adds empty work positions)
  *   out           device, bf16 [Tq, Hq, D]; rows not covered by cu_seqlens_q
  *                 are left untouched
  * D in {64, 128}; Hq / Hkv in {1, 2, 4, 8}; bs a multiple of 16.  No
