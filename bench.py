@@ -2,24 +2,33 @@
 
 A step is the whole hot path on one batch: store_kvcache of the step's new
 tokens, then paged_attn_decode (stream-K decode kernel + log-sum-exp merge).
-The workload is the Qwen3-0.6B-shaped serving step: 64 sequences, 16 query /
-8 KV heads, head_dim 128, block_size 256, context lengths uniform in
-[128, 4096], shuffled physical blocks, bf16 N(0,1) data (seeded, synthetic).
-Its K/V (about 0.55 GB per step) is larger than the 129 MB L2, so no flush
-is needed between steps.
+The default workload is the max-concurrency serving step: 512 sequences
+(max_num_seqs), 16 query / 8 KV heads, head_dim 128, block_size 256, context
+lengths round(exp(U[ln 16, ln 4096])) (max_model_len 4096), shuffled
+physical blocks, bf16 N(0,1) data (seeded, synthetic), and a store of 512
+new tokens of which 26 carry the padding slot -1.  Its K/V (about 1.5 GB per
+step) is far larger than the 129 MB L2, so no flush is needed between steps.
 
 Prints one JSON line.  `value` is the step's algorithmic bytes (K/V over
 every context, q, out, block-table entries, context_lens, plus the store's
 rows and slots) divided by the device time per step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME]
+
+--config picks another decode workload (a parity case, not the headline):
+tiny_paged_decode, qwen3_0p6b_decode, vllm_bs16_8b_heads, max_concurrency
+(default), long_context_shared_prefix; an index 0-4 works too.
 
 Two further lines measure the paths built beside the decode step (not the
 headline):
     --kv-dtype fp8     the same decode step over FP8 (E4M3) caches
     --path prefill     a 16384-token paged prefill step (store + causal
                        attention through block tables), against the bf16
-                       tensor roofline
+                       tensor roofline; --config then names a prefill
+                       workload (tiny_paged_prefill, qwen3_prefill_16k
+                       (default), vllm_bs16_prefill_ragged,
+                       shared_prefix_prefill)
 """
 
 from __future__ import annotations
@@ -40,13 +49,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: KV GB/s & % of HBM peak; seq-steps/s (1×GB300)"
-WORKLOAD_IDX = 1  # the Qwen3-0.6B-shaped step
+DECODE_WORKLOAD = "max_concurrency"  # 512 seqs, 16Q/8KV, D128, bs256, ctx logU[16, 4096]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_METRIC = "paged prefill attention: TFLOP/s & % of bf16 tensor peak; tokens/s (1×GB300)"
 FP8_METRIC = "paged decode attention, FP8 (E4M3) KV cache: KV GB/s & % of HBM peak (1×GB300)"
-PREFILL_IDX = 1  # the 16384-token Qwen3-0.6B-shaped prefill step
+PREFILL_WORKLOAD = "qwen3_prefill_16k"  # the 16384-token Qwen3-0.6B-shaped prefill step
+CPU_BUDGET_S = 8.0  # seconds of oracle work per cpu_baseline run (one core, then all cores)
 PREFILL_SOURCES = ["pkv_prefill_tc.cuh", "pkv_prefill.h", "pkv_tc.cuh", "pkv_kernels.h", "pkv_ptx.cuh"]
 DECODE_SOURCES = ["pkv_decode.cuh", "pkv_merge.cu", "pkv_kernels.h", "pkv_ptx.cuh"]
 
@@ -61,12 +71,79 @@ def parse_args(argv=None):
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="decode over bf16 or FP8 (E4M3) caches")
     ap.add_argument("--path", choices=["decode", "prefill"], default="decode")
-    ap.add_argument("--config", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--config", default=None,
+                    help="workload name (or index): decode tiny_paged_decode, qwen3_0p6b_decode, "
+                         "vllm_bs16_8b_heads, max_concurrency (default), "
+                         "long_context_shared_prefix; prefill tiny_paged_prefill, "
+                         "qwen3_prefill_16k (default), vllm_bs16_prefill_ragged, "
+                         "shared_prefix_prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
 # ----------------------------------------------------------------- helpers
+
+
+def config_index(arg, names, default: str) -> int:
+    """Index of a workload given by name or number (None = the default)."""
+    if arg is None:
+        return names.index(default)
+    if isinstance(arg, int) or str(arg).isdigit():
+        idx = int(arg)
+        if not 0 <= idx < len(names):
+            raise SystemExit(f"--config {arg}: no such workload (0..{len(names) - 1})")
+        return idx
+    if arg not in names:
+        raise SystemExit(f"--config {arg}: not one of {', '.join(names)}")
+    return names.index(arg)
+
+
+def decode_workload(args):
+    from paged_kv_cache_85_gb300 import workload as wl
+
+    return wl.config_workload(config_index(args.config, wl.CONFIG_NAMES, DECODE_WORKLOAD))
+
+
+def prefill_workload(args):
+    from paged_kv_cache_85_gb300 import workload as wl
+
+    return wl.prefill_config_workload(
+        config_index(args.config, wl.PREFILL_CONFIG_NAMES, PREFILL_WORKLOAD))
+
+
+def decode_config(w, kv_dtype: str, world: int) -> dict:
+    """The `config` object of a decode line: the workload itself, identical
+    for both arms (nothing about how either arm runs it)."""
+    eb = 1 if kv_dtype == "fp8" else 2
+    cfg = {
+        "workload": w.name + ("_fp8" if kv_dtype == "fp8" else ""),
+        "num_seqs": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
+        "block_size": w.bs, "context_lens": w.context_lens_summary(),
+        "num_blocks": w.NB, "max_blocks_per_seq": w.MBS,
+        "new_tokens_per_step": w.N, "padding_slots": int((w.slot_mapping < 0).sum()),
+        "step_bytes": w.decode_bytes(eb) + w.store_bytes(eb), "kv_bytes": w.kv_bytes(eb),
+        "kv_cache_dtype": kv_dtype,
+        "l2": "inputs larger than L2 (no flush)" if w.kv_bytes(eb) > 4 * 129e6
+              else "inputs smaller than L2 (no flush; launch-bound)",
+        "parallelism": "replicas" if world > 1 else "single GPU",
+    }
+    uniq = w.unique_kv_bytes() * eb // 2
+    if uniq != w.kv_bytes(eb):
+        cfg["unique_kv_bytes"] = uniq
+    return cfg
+
+
+def prefill_config(w, world: int) -> dict:
+    """The `config` object of a prefill line, identical for both arms."""
+    return {
+        "workload": w.name, "num_seqs": w.B, "new_tokens": w.Tq,
+        "q_lens": sorted(set(int(x) for x in w.q_lens))[:8],
+        "cached_lens": [int(x) for x in (w.k_lens - w.q_lens)][:16],
+        "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs,
+        "causal_flops": w.flops(), "kv_bytes": w.kv_bytes(),
+        "l2": "q + K/V + out per step exceed L2 (no flush)",
+        "parallelism": "replicas" if world > 1 else "single GPU",
+    }
 
 
 def load_peaks():
@@ -241,18 +318,20 @@ def barrier(dist, device=None):
 # ----------------------------------------------------------- CPU oracle leg
 
 
-def oracle_sample(w, seqs, kc, vc):
+def oracle_sample(w, seqs, kc, vc, threads=1):
     """Run the oracle's store + decode on sequences `seqs` of the step; return bytes moved.
 
     `kc`, `vc` are the oracle's own copies of the caches (the store writes
-    them in place, as the GPU path does).
+    them in place, as the GPU path does).  The (sequence, head) rows are split
+    over `threads` host threads.
     """
     import oracle
 
     sel = np.asarray(seqs)
     oracle.store_kvcache_(w.k_new[sel], w.v_new[sel], kc, vc, w.slot_mapping[sel])
     pairs = np.array([(b, h) for b in sel for h in range(w.Hq)], np.int32)
-    oracle.paged_attn_decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, pairs=pairs)
+    oracle.paged_attn_decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, pairs=pairs,
+                             threads=threads)
     return sample_bytes(w, sel)
 
 
@@ -266,24 +345,48 @@ def sample_bytes(w, sel):
     return kv + qo + tab + store
 
 
-def time_oracle(w, budget_s: float):
+def calibrate(run, n_max: int, budget_s: float, threads: int) -> int:
+    """How many units (a prefix of the step) fill about `budget_s` seconds:
+    time a probe of a few units per thread, then scale."""
+    probe = int(max(1, min(n_max, 2 * threads)))
+    t0 = time.perf_counter()
+    run(probe)
+    per = max(time.perf_counter() - t0, 1e-4) / probe
+    return int(max(1, min(n_max, budget_s / per)))
+
+
+def time_oracle(w, budget_s: float, threads: int = 1):
     """Time the oracle on a bounded sample (a prefix of the sequences) of the step."""
     kc, vc = w.k_cache.copy(), w.v_cache.copy()
-    t0 = time.perf_counter()
     oracle_sample(w, [0], kc, vc)  # also compiles / loads the oracle
-    one = max(time.perf_counter() - t0, 1e-4)
-    m = int(max(1, min(w.B, budget_s / one)))
+    m = calibrate(lambda n: oracle_sample(w, list(range(n)), kc, vc, threads), w.B, budget_s,
+                  threads)
     t0 = time.perf_counter()
-    nbytes = oracle_sample(w, list(range(m)), kc, vc)
+    nbytes = oracle_sample(w, list(range(m)), kc, vc, threads)
     dt = time.perf_counter() - t0
     return {
         "value": nbytes / dt / 1e9,
         "unit": "GB/s",
-        "cores": 1,
+        "cores": threads,
         "kind": "oracle",
         "sample": f"store+decode of the first {m} of {w.B} sequences (all heads), fp64 C oracle, "
-                  f"single thread, {dt:.1f} s",
+                  f"{threads} thread{'s' if threads > 1 else ''}, {dt:.1f} s",
     }
+
+
+def cpu_baselines(timer, budget_s: float = CPU_BUDGET_S) -> dict:
+    """The oracle timed on one host core, then on all of them; the all-cores
+    run is the headline object, both runs are listed under `by_cores`."""
+    import oracle
+
+    n = oracle.host_cores()
+    runs = [timer(budget_s, 1)]
+    if n > 1:
+        runs.append(timer(budget_s, n))
+    top = dict(runs[-1])
+    top["host_cores"] = n
+    top["by_cores"] = runs
+    return top
 
 
 def compact_sample(w, m):
@@ -305,35 +408,42 @@ def compact_sample(w, m):
     return ids, tables, slots
 
 
-def time_oracle_fp8(w, budget_s: float, k_scale: float, v_scale: float):
-    """Time the FP8 oracle (quantizing store + decode over dequantized caches)
-    on the first m sequences of the step, their blocks gathered compactly."""
+def fp8_sample_bytes(w, m):
+    ctx = w.context_lens[:m].astype(np.int64)
+    return (int(ctx.sum()) * w.Hkv * w.D * 2 + 2 * m * w.Hq * w.D * 2
+            + int(((ctx + w.bs - 1) // w.bs).sum()) * 4 + 4 * m
+            + int((w.slot_mapping[:m] >= 0).sum()) * w.Hkv * w.D * 3 * 2 + 8 * m)
+
+
+def oracle_sample_fp8(w, m, k_scale, v_scale, threads=1):
+    """FP8 oracle (quantizing store + decode over dequantized caches) on the
+    first m sequences of the step, their blocks gathered compactly; returns
+    (seconds of the store + decode, bytes)."""
     import oracle
 
-    def run(m):
-        ids, tables, slots = compact_sample(w, m)
-        kc = oracle.quantize_bf16(w.k_cache[ids], k_scale)
-        vc = oracle.quantize_bf16(w.v_cache[ids], v_scale)
-        t0 = time.perf_counter()
-        kc, vc, _ = oracle.store_kvcache_fp8(w.k_new[:m], w.v_new[:m], kc, vc, slots, k_scale, v_scale)
-        oracle.paged_attn_decode_fp8(w.q[:m], kc, vc, tables, w.context_lens[:m], w.scale,
-                                     k_scale, v_scale)
-        return time.perf_counter() - t0
+    ids, tables, slots = compact_sample(w, m)
+    kc = oracle.quantize_bf16(w.k_cache[ids], k_scale)
+    vc = oracle.quantize_bf16(w.v_cache[ids], v_scale)
+    t0 = time.perf_counter()
+    kc, vc, _ = oracle.store_kvcache_fp8(w.k_new[:m], w.v_new[:m], kc, vc, slots, k_scale, v_scale)
+    oracle.paged_attn_decode_fp8(w.q[:m], kc, vc, tables, w.context_lens[:m], w.scale,
+                                 k_scale, v_scale, threads=threads)
+    return time.perf_counter() - t0, fp8_sample_bytes(w, m)
 
-    one = max(run(1), 1e-4)
-    m = int(max(1, min(w.B, budget_s / one)))
-    dt = run(m)
-    ctx = w.context_lens[:m].astype(np.int64)
-    nbytes = (int(ctx.sum()) * w.Hkv * w.D * 2 + 2 * m * w.Hq * w.D * 2
-              + int(((ctx + w.bs - 1) // w.bs).sum()) * 4 + 4 * m
-              + int((w.slot_mapping[:m] >= 0).sum()) * w.Hkv * w.D * 3 * 2 + 8 * m)
+
+def time_oracle_fp8(w, budget_s: float, k_scale: float, v_scale: float, threads: int = 1):
+    """Time the FP8 oracle on the first m sequences of the step."""
+    m = calibrate(lambda n: oracle_sample_fp8(w, n, k_scale, v_scale, threads), w.B, budget_s,
+                  threads)
+    dt, nbytes = oracle_sample_fp8(w, m, k_scale, v_scale, threads)
     return {
         "value": nbytes / dt / 1e9,
         "unit": "GB/s",
-        "cores": 1,
+        "cores": threads,
         "kind": "oracle",
         "sample": f"FP8 store+decode of the first {m} of {w.B} sequences (all heads), fp64 C "
-                  f"oracle over dequantized caches, single thread, {dt:.1f} s",
+                  f"oracle over dequantized caches, {threads} thread{'s' if threads > 1 else ''}, "
+                  f"{dt:.1f} s",
     }
 
 
@@ -351,28 +461,32 @@ def prefill_pair_flops(w, pairs):
     return int(4 * w.D * (pos + 1).sum())
 
 
-def time_oracle_prefill(w, budget_s: float):
+def time_oracle_prefill(w, budget_s: float, threads: int = 1, caches=None):
     import oracle
 
-    kc, vc = w.k_cache.copy(), w.v_cache.copy()
-    oracle.store_kvcache_(w.k_new, w.v_new, kc, vc, w.slot_mapping)
-    probe = prefill_sample_pairs(w, 64)
+    if caches is None:
+        kc, vc = w.k_cache.copy(), w.v_cache.copy()
+        oracle.store_kvcache_(w.k_new, w.v_new, kc, vc, w.slot_mapping)
+    else:
+        kc, vc = caches
+    probe = prefill_sample_pairs(w, 64 * threads)
     t0 = time.perf_counter()
     oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k, w.scale,
-                         pairs=probe)
+                         pairs=probe, threads=threads)
     per_pair = max(time.perf_counter() - t0, 1e-4) / len(probe)
     pairs = prefill_sample_pairs(w, int(budget_s / per_pair))
     t0 = time.perf_counter()
     oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k, w.scale,
-                         pairs=pairs)
+                         pairs=pairs, threads=threads)
     dt = time.perf_counter() - t0
     return {
         "value": prefill_pair_flops(w, pairs) / dt / 1e12,
         "unit": "TFLOP/s",
-        "cores": 1,
+        "cores": threads,
         "kind": "oracle",
         "sample": f"causal attention of {len(pairs)} (token, head) rows spread over the "
-                  f"{w.Tq}-token step, fp64 C oracle, single thread, {dt:.1f} s",
+                  f"{w.Tq}-token step, fp64 C oracle, {threads} thread{'s' if threads > 1 else ''}, "
+                  f"{dt:.1f} s",
     }
 
 
@@ -392,7 +506,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     pkv.load_library()
 
-    w = wl.config_workload(WORKLOAD_IDX if args.config is None else args.config)
+    w = decode_workload(args)
     fp8 = args.kv_dtype == "fp8"
     eb = 1 if fp8 else 2
     step_bytes = w.decode_bytes(eb) + w.store_bytes(eb)
@@ -529,7 +643,31 @@ def run_ours(args):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle_fp8(w, 12.0, k_scale, v_scale) if fp8 else time_oracle(w, budget_s=12.0)
+        if fp8:
+            cpu = cpu_baselines(lambda b, t: time_oracle_fp8(w, b, k_scale, v_scale, t))
+        else:
+            cpu = cpu_baselines(lambda b, t: time_oracle(w, b, t))
+
+    roofline = {
+        "kernel": "paged_attn_decode (stream-K decode kernel + LSE merge)",
+        "bound": "hbm",
+        "achieved": round(achieved, 1),
+        "peak": peak,
+        "unit": "GB/s",
+        "frac": round(achieved / peak, 4),
+        "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
+        "traffic": profiled_traffic(w.name, "paged_decode_fp8" if fp8 else "paged_decode"),
+        "algorithmic_bytes_per_launch": w.decode_bytes(eb),
+        "us_per_launch": round(ms_attn * 1e3, 2),
+    }
+    cfg = decode_config(w, args.kv_dtype, world)
+    if "unique_kv_bytes" in cfg:
+        # shared prefix blocks: the same rate counted on the distinct blocks read
+        uniq_bytes = w.decode_bytes(eb) - w.kv_bytes(eb) + cfg["unique_kv_bytes"]
+        ach_u = uniq_bytes / (ms_attn * 1e-3) / 1e9
+        roofline["unique_bytes_per_launch"] = uniq_bytes
+        roofline["achieved_unique"] = round(ach_u, 1)
+        roofline["frac_unique"] = round(ach_u / peak, 4)
 
     line = {
         "metric": FP8_METRIC if fp8 else METRIC,
@@ -545,17 +683,8 @@ def run_ours(args):
         "dtype": "fp8-e4m3 KV (e4m3/f16 MMA, fp32 accumulate)" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)" +
                 (", caches quantized to E4M3 with per-tensor amax/448 scales" if fp8 else ""),
-        "config": {
-            "workload": w.name + ("_fp8" if fp8 else ""),
-            "num_seqs": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
-            "block_size": w.bs, "context_lens": "uniform [128, 4096]",
-            "num_blocks": w.NB, "max_blocks_per_seq": w.MBS,
-            "new_tokens_per_step": w.N, "max_ctas": args.max_ctas or "one per SM",
-            "step_bytes": step_bytes, "kv_bytes": w.kv_bytes(eb),
-            "kv_cache_dtype": args.kv_dtype,
-            "l2": "inputs larger than L2 (no flush)",
-            "parallelism": "replicas" if world > 1 else "single GPU",
-        },
+        "config": cfg,
+        "launch": {"max_ctas": args.max_ctas or "as many as fit on the device"},
         "us_per_step": round(ms_step * 1e3, 2),
         "seq_steps_per_s": round(world * w.B / (ms_step * 1e-3), 1),
         "pct_of_hbm_peak": {
@@ -563,18 +692,7 @@ def run_ours(args):
             "nominal_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 1),
             "peak_source": peak_src,
         },
-        "roofline": {
-            "kernel": "paged_attn_decode (stream-K decode kernel + LSE merge)",
-            "bound": "hbm",
-            "achieved": round(achieved, 1),
-            "peak": peak,
-            "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
-            "traffic": profiled_traffic(w.name, "paged_decode_fp8" if fp8 else "paged_decode"),
-            "algorithmic_bytes_per_launch": w.decode_bytes(eb),
-            "us_per_launch": round(ms_attn * 1e3, 2),
-        },
+        "roofline": roofline,
         "e2e": {
             "value": round(job_throughput(step_bytes, world, ms_e2e), 2),
             "unit": "GB/s",
@@ -607,7 +725,7 @@ def run_ours_prefill(args):
     torch.cuda.set_device(dev)
     pkv.load_library()
 
-    w = wl.prefill_config_workload(PREFILL_IDX if args.config is None else args.config)
+    w = prefill_workload(args)
     flops = w.flops()
 
     def bf(a):
@@ -695,7 +813,11 @@ def run_ours_prefill(args):
         return None
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle_prefill(w, budget_s=12.0)
+        import oracle
+
+        kc_o, vc_o = w.k_cache.copy(), w.v_cache.copy()
+        oracle.store_kvcache_(w.k_new, w.v_new, kc_o, vc_o, w.slot_mapping)
+        cpu = cpu_baselines(lambda b, t: time_oracle_prefill(w, b, t, caches=(kc_o, vc_o)))
     line = {
         "metric": PREFILL_METRIC,
         "value": round(value, 2),
@@ -709,15 +831,7 @@ def run_ours_prefill(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks, cached prefixes)",
-        "config": {
-            "workload": w.name, "num_seqs": w.B, "new_tokens": w.Tq,
-            "q_lens": sorted(set(int(x) for x in w.q_lens))[:8],
-            "cached_lens": [int(x) for x in (w.k_lens - w.q_lens)][:16],
-            "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs,
-            "causal_flops": flops, "kv_bytes": w.kv_bytes(),
-            "l2": "q + K/V + out per step exceed L2 (no flush)",
-            "parallelism": "replicas" if world > 1 else "single GPU",
-        },
+        "config": prefill_config(w, world),
         "us_per_step": round(ms_step * 1e3, 2),
         "tokens_per_s": round(world * w.Tq / (ms_step * 1e-3), 1),
         "roofline": {
@@ -755,52 +869,69 @@ def run_ours_prefill(args):
 # ----------------------------------------------------------- reference arm
 
 
+def reference_line(args, metric, unit, value, dt, cfg, threads, sample, ndigits):
+    v = round(value, ndigits)
+    return {
+        "metric": metric, "value": v, "unit": unit,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)",
+        "config": cfg,
+        "impl": "reference",
+        "cpu_baseline": {"value": v, "unit": unit, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args):
-    """The oracle as the reference arm: K timed steps of a bounded sample on host cores."""
+    """The oracle as the reference arm: K timed steps of a bounded sample of
+    the same workload, on all host cores."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
-    from paged_kv_cache_85_gb300 import workload as wl
+    import oracle
 
-    w = wl.config_workload(WORKLOAD_IDX if args.config is None else args.config)
-    kc, vc = w.k_cache.copy(), w.v_cache.copy()
-    t0 = time.perf_counter()
-    oracle_sample(w, [0], kc, vc)
-    one = max(time.perf_counter() - t0, 1e-4)
+    w = decode_workload(args)
+    threads = oracle.host_cores()
     budget = 150.0 / max(1, args.steps + args.warmup)
-    m = int(max(1, min(w.B, budget / one)))
-    seqs = list(range(m))
-    for _ in range(args.warmup):
-        oracle_sample(w, seqs, kc, vc)
-    t0 = time.perf_counter()
-    nbytes = 0
-    for _ in range(args.steps):
-        nbytes += oracle_sample(w, seqs, kc, vc)
-    dt = time.perf_counter() - t0
-    value = nbytes / dt / 1e9
-    sample = (f"each step: store+decode of the first {m} of {w.B} sequences (all heads), "
-              f"fp64 C oracle, single thread")
-    line = {
-        "metric": METRIC,
-        "value": round(value, 4),
-        "unit": "GB/s",
-        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(1e3 * dt / args.steps, 3),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)",
-        "config": {"workload": w.name, "num_seqs": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
-                   "head_dim": w.D, "block_size": w.bs},
-        "impl": "reference",
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }
+    fp8 = args.kv_dtype == "fp8"
+    if fp8:
+        from paged_kv_cache_85_gb300 import workload as wl
+
+        def amax(a, b):
+            return float(np.abs(wl.bf16_bits_to_f32(np.concatenate([a.ravel(), b.ravel()]))).max())
+
+        ks, vs = amax(w.k_cache, w.k_new) / 448.0, amax(w.v_cache, w.v_new) / 448.0
+        m = calibrate(lambda n: oracle_sample_fp8(w, n, ks, vs, threads), w.B, budget, threads)
+        for _ in range(args.warmup):
+            oracle_sample_fp8(w, m, ks, vs, threads)
+        dt, nbytes = 0.0, 0
+        for _ in range(args.steps):
+            t, nb = oracle_sample_fp8(w, m, ks, vs, threads)
+            dt += t
+            nbytes += nb
+        what = "FP8 store+decode"
+    else:
+        kc, vc = w.k_cache.copy(), w.v_cache.copy()
+        oracle_sample(w, [0], kc, vc)
+        m = calibrate(lambda n: oracle_sample(w, list(range(n)), kc, vc, threads), w.B, budget,
+                      threads)
+        seqs = list(range(m))
+        for _ in range(args.warmup):
+            oracle_sample(w, seqs, kc, vc, threads)
+        t0 = time.perf_counter()
+        nbytes = 0
+        for _ in range(args.steps):
+            nbytes += oracle_sample(w, seqs, kc, vc, threads)
+        dt = time.perf_counter() - t0
+        what = "store+decode"
+    sample = (f"each step: {what} of the first {m} of {w.B} sequences (all heads), "
+              f"fp64 C oracle, {threads} host threads")
+    line = reference_line(args, FP8_METRIC if fp8 else METRIC, "GB/s", nbytes / dt / 1e9, dt,
+                          decode_config(w, args.kv_dtype, int(os.environ.get("WORLD_SIZE", "1"))),
+                          threads, sample, 4)
     print(json.dumps(line), flush=True)
     return line
 
@@ -811,22 +942,22 @@ def run_reference_prefill(args):
     if rank != 0:
         return None
     import oracle
-    from paged_kv_cache_85_gb300 import workload as wl
 
-    w = wl.prefill_config_workload(PREFILL_IDX if args.config is None else args.config)
+    w = prefill_workload(args)
+    threads = oracle.host_cores()
     kc, vc = w.k_cache.copy(), w.v_cache.copy()
     oracle.store_kvcache_(w.k_new, w.v_new, kc, vc, w.slot_mapping)
-    probe = prefill_sample_pairs(w, 64)
+    probe = prefill_sample_pairs(w, 64 * threads)
     t0 = time.perf_counter()
     oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k, w.scale,
-                         pairs=probe)
+                         pairs=probe, threads=threads)
     per_pair = max(time.perf_counter() - t0, 1e-4) / len(probe)
     budget = 150.0 / max(1, args.steps + args.warmup)
     pairs = prefill_sample_pairs(w, max(w.Hq, int(budget / per_pair)))
 
     def one():
         oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k,
-                             w.scale, pairs=pairs)
+                             w.scale, pairs=pairs, threads=threads)
 
     for _ in range(args.warmup):
         one()
@@ -836,21 +967,11 @@ def run_reference_prefill(args):
     dt = time.perf_counter() - t0
     value = prefill_pair_flops(w, pairs) * args.steps / dt / 1e12
     sample = (f"each step: causal attention of {len(pairs)} (token, head) rows spread over the "
-              f"{w.Tq}-token step, fp64 C oracle, single thread")
-    line = {
-        "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
-        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks, cached prefixes)",
-        "config": {"workload": w.name, "num_seqs": w.B, "new_tokens": w.Tq, "q_heads": w.Hq,
-                   "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs},
-        "impl": "reference",
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1,
-                         "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }
+              f"{w.Tq}-token step, fp64 C oracle, {threads} host threads")
+    line = reference_line(args, PREFILL_METRIC, "TFLOP/s", value, dt,
+                          prefill_config(w, int(os.environ.get("WORLD_SIZE", "1"))),
+                          threads, sample, 6)
+    line["data"] = "synthetic (seeded N(0,1) bf16, shuffled physical blocks, cached prefixes)"
     print(json.dumps(line), flush=True)
     return line
 

@@ -15,6 +15,7 @@ import ctypes
 import os
 import subprocess
 import threading
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -82,6 +83,36 @@ def _ptr(a: np.ndarray):
     return ctypes.c_void_p(a.ctypes.data)
 
 
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _run_pairs(call, pairs: np.ndarray, out: np.ndarray, threads: int) -> int:
+    """Run ``call(pairs_chunk, out_chunk) -> status`` over disjoint chunks of
+    the (row, head) pairs, on up to ``threads`` host threads.
+
+    Each pair's result depends only on the inputs, so splitting the pair list
+    changes nothing in the arithmetic: the C routine computes every row on its
+    own, and ctypes releases the GIL while it runs.  Returns the smallest
+    status (negative = an allocation failed in some chunk).
+    """
+    n = pairs.shape[0]
+    threads = max(1, min(int(threads), n))
+    if threads == 1:
+        return int(call(pairs, out))
+    # more chunks than threads, so that uneven rows (long and short contexts) balance
+    bounds = np.linspace(0, n, 4 * threads + 1).astype(np.int64)
+    chunks = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        res = list(ex.map(lambda ab: int(call(np.ascontiguousarray(pairs[ab[0]:ab[1]]),
+                                              out[ab[0]:ab[1]])), chunks))
+    return min(res)
+
+
 def _c(a, dtype):
     a = np.ascontiguousarray(a, dtype=dtype)
     return a
@@ -126,11 +157,13 @@ def store_kvcache_(k, v, k_cache, v_cache, slot_mapping) -> int:
                                         _ptr(slots), N, Hkv, D, NB, bs))
 
 
-def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, pairs=None):
+def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, pairs=None,
+                      threads=1):
     """fp64 decode attention.
 
     Without ``pairs`` returns ``[B, Hq, D]``; with ``pairs`` (an ``[n, 2]``
-    array of (b, h)) returns ``[n, D]`` for just those rows.
+    array of (b, h)) returns ``[n, D]`` for just those rows.  ``threads > 1``
+    splits the pairs over host threads (same results).
     """
     lib = _load()
     q = _c(q, np.uint16)
@@ -149,9 +182,11 @@ def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, pa
     else:
         pr = _c(pairs, np.int32).reshape(-1, 2)
         out = np.zeros((pr.shape[0], D), dtype=np.float64)
-        bad = lib.oracle_paged_attn_decode_pairs(
-            _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), MBS, _ptr(cl), B, Hq, Hkv, D, NB, bs,
-            float(scale), _ptr(pr), pr.shape[0], _ptr(out))
+        bad = _run_pairs(
+            lambda pc, oc: lib.oracle_paged_attn_decode_pairs(
+                _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), MBS, _ptr(cl), B, Hq, Hkv, D, NB, bs,
+                float(scale), _ptr(pc), pc.shape[0], _ptr(oc)),
+            pr, out, threads)
     if bad < 0:
         raise MemoryError("oracle allocation failed")
     return out
@@ -226,7 +261,8 @@ def dequant_fp8(codes, scale):
     return out
 
 
-def paged_attn_decode_values(q, k_vals, v_vals, block_tables, context_lens, scale, pairs=None):
+def paged_attn_decode_values(q, k_vals, v_vals, block_tables, context_lens, scale, pairs=None,
+                             threads=1):
     """fp64 decode attention over caches holding fp64 values [NB, bs, Hkv, D]."""
     lib = _load()
     q = _c(q, np.uint16)
@@ -242,33 +278,37 @@ def paged_attn_decode_values(q, k_vals, v_vals, block_tables, context_lens, scal
     else:
         pr = _c(pairs, np.int32).reshape(-1, 2)
     out = np.zeros((pr.shape[0], D), dtype=np.float64)
-    bad = lib.oracle_paged_attn_decode_pairs_f64kv(
-        _ptr(q), _ptr(kv), _ptr(vv), _ptr(bt), bt.shape[1], _ptr(cl), Hq, Hkv, D, NB, bs,
-        float(scale), _ptr(pr), pr.shape[0], _ptr(out))
+    bad = _run_pairs(
+        lambda pc, oc: lib.oracle_paged_attn_decode_pairs_f64kv(
+            _ptr(q), _ptr(kv), _ptr(vv), _ptr(bt), bt.shape[1], _ptr(cl), Hq, Hkv, D, NB, bs,
+            float(scale), _ptr(pc), pc.shape[0], _ptr(oc)),
+        pr, out, threads)
     if bad < 0:
         raise MemoryError("oracle allocation failed")
     return out.reshape(B, Hq, D) if pairs is None else out
 
 
 def paged_attn_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale,
-                          v_scale, pairs=None):
+                          v_scale, pairs=None, threads=1):
     """fp64 decode attention over FP8 caches (dequantized K and V)."""
     kd = dequant_fp8(k_cache, k_scale)
     vd = dequant_fp8(v_cache, v_scale)
-    return paged_attn_decode_values(q, kd, vd, block_tables, context_lens, scale, pairs=pairs)
+    return paged_attn_decode_values(q, kd, vd, block_tables, context_lens, scale, pairs=pairs,
+                                    threads=threads)
 
 
 # ---------------------------------------------------------------- prefill
 
 
 def paged_prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k, scale,
-                  pairs=None):
+                  pairs=None, threads=1):
     """fp64 causal prefill attention over the paged cache.
 
     q is [Tq, Hq, D] (the sequences' new tokens, concatenated); query i of
     sequence b sits at position k_len_b - q_len_b + i and attends to positions
     0 .. that one.  Returns [Tq, Hq, D], or [len(pairs), D] for the listed
-    (token row, head) pairs.
+    (token row, head) pairs.  ``threads > 1`` splits the pairs over host
+    threads (same results).
     """
     lib = _load()
     q = _c(q, np.uint16)
@@ -287,9 +327,11 @@ def paged_prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k,
     else:
         pr = _c(pairs, np.int32).reshape(-1, 2)
     out = np.zeros((pr.shape[0], D), dtype=np.float64)
-    bad = lib.oracle_paged_prefill_pairs(
-        _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cq), _ptr(ck), B, Hq, Hkv, D,
-        NB, bs, float(scale), _ptr(pr), pr.shape[0], _ptr(out))
+    bad = _run_pairs(
+        lambda pc, oc: lib.oracle_paged_prefill_pairs(
+            _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cq), _ptr(ck), B, Hq, Hkv,
+            D, NB, bs, float(scale), _ptr(pc), pc.shape[0], _ptr(oc)),
+        pr, out, threads)
     if bad < 0:
         raise MemoryError("oracle allocation failed")
     return out.reshape(Tq, Hq, D) if pairs is None else out

@@ -76,10 +76,17 @@ class Workload:
     v_new: np.ndarray  # u16 bf16 [N, Hkv, D]
     slot_mapping: np.ndarray  # int64 [N]; -1 = padding, skipped
     recipe: str = ""
+    ctx_dist: str = ""  # how context_lens were drawn, e.g. "uniform [128, 4096]"
 
     @property
     def G(self) -> int:
         return self.Hq // self.Hkv
+
+    def context_lens_summary(self) -> dict:
+        """The drawn context lengths: distribution and realised statistics."""
+        c = self.context_lens.astype(np.int64)
+        return {"dist": self.ctx_dist or "given", "min": int(c.min()), "max": int(c.max()),
+                "mean": round(float(c.mean()), 1), "total_tokens": int(c.sum())}
 
     @property
     def N(self) -> int:
@@ -142,6 +149,7 @@ def make_workload(
     poison_unused: bool = False,
     recipe: str = "",
     rng: np.random.Generator | None = None,
+    ctx_dist: str = "",
 ) -> Workload:
     """Draw one step's inputs.
 
@@ -191,7 +199,7 @@ def make_workload(
         name=name, B=B, Hq=Hq, Hkv=Hkv, D=D, bs=bs, NB=NB, MBS=MBS,
         scale=float(np.float32(1.0 / math.sqrt(D))),
         context_lens=ctx, block_tables=tables, q=q, k_cache=k_cache, v_cache=v_cache,
-        k_new=k_new, v_new=v_new, slot_mapping=slots, recipe=recipe,
+        k_new=k_new, v_new=v_new, slot_mapping=slots, recipe=recipe, ctx_dist=ctx_dist,
     )
 
 
@@ -226,34 +234,35 @@ def config_workload(idx: int, seed: int = 0, poison_unused: bool = False) -> Wor
     if idx == 0:
         return make_workload(
             name, B=4, Hq=4, Hkv=2, D=64, bs=16, context_lens=[1, 17, 40, 300], NB=64,
-            rng=rng, poison_unused=poison_unused,
+            rng=rng, poison_unused=poison_unused, ctx_dist="fixed {1, 17, 40, 300}",
             recipe="4 seqs, ctx {1,17,40,300}, bs16, 4Q/2KV, D64, NB=64 permuted, N(0,1) bf16",
         )
     if idx == 1:
         ctx = rng.integers(128, 4096, size=64, endpoint=True)
         return make_workload(
             name, B=64, Hq=16, Hkv=8, D=128, bs=256, context_lens=ctx, rng=rng,
-            poison_unused=poison_unused,
+            poison_unused=poison_unused, ctx_dist="uniform integers [128, 4096]",
             recipe="64 seqs, ctx U[128,4096], bs256, 16Q/8KV, D128, NB=ceil(1.25*used), N(0,1) bf16",
         )
     if idx == 2:
         ctx = rng.integers(1, 2048, size=256, endpoint=True)
         return make_workload(
             name, B=256, Hq=32, Hkv=8, D=128, bs=16, context_lens=ctx, rng=rng,
-            poison_unused=poison_unused,
+            poison_unused=poison_unused, ctx_dist="uniform integers [1, 2048]",
             recipe="256 seqs, ctx U[1,2048], bs16, 32Q/8KV, D128, NB=ceil(1.25*used), N(0,1) bf16",
         )
     if idx == 3:
         ctx = np.rint(np.exp(rng.uniform(math.log(16), math.log(4096), size=512))).astype(np.int64)
         return make_workload(
             name, B=512, Hq=16, Hkv=8, D=128, bs=256, context_lens=ctx, rng=rng, pad_frac=0.05,
-            poison_unused=poison_unused,
+            poison_unused=poison_unused, ctx_dist="round(exp(uniform [ln 16, ln 4096]))",
             recipe="512 seqs, ctx logU[16,4096], bs256, 16Q/8KV, D128, 26 slots=-1, N(0,1) bf16",
         )
     if idx == 4:
         return make_workload(
             name, B=8, Hq=32, Hkv=8, D=128, bs=256, context_lens=[32768] * 8,
             shared_prefix_tokens=8192, rng=rng, poison_unused=poison_unused,
+            ctx_dist="fixed 32768, first 8192 tokens' blocks shared by all tables",
             recipe="8 seqs x 32768, bs256, 32Q/8KV, D128, first 8192 tokens' blocks shared",
         )
     raise ValueError(f"no config {idx}")
