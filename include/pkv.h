@@ -32,12 +32,16 @@
  *
  * Conventions common to every call:
  *   - Every tensor pointer is a DEVICE pointer owned by the caller; the
- *     library never allocates, frees or keeps device memory.
+ *     library never allocates or frees device memory.  The one piece of
+ *     device memory it keeps is the fixed scratch array of
+ *     pkv_paged_attn_decode_noalloc (PKV_NOALLOC_SCRATCH_BYTES, a static
+ *     __device__ array held by every GPU that loads the library).
  *   - Tensors are dense row-major; bf16 data is passed as `const void *`.
  *     Every pointer must be 16-byte aligned.
- *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
- *     only enqueue work: they never synchronise the host and never allocate,
- *     so they can be captured into a CUDA graph.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *     pkv_store_kvcache, pkv_paged_attn_decode, pkv_paged_prefill and the FP8
+ *     calls only enqueue work: they never synchronise the host and never
+ *     allocate, so they can be captured into a CUDA graph.
  *   - Argument errors are reported by the return status before any launch;
  *     pkv_last_error() then gives a message.  Data errors found on the
  *     device (an out-of-range slot or block id, a context length above
@@ -119,10 +123,12 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int MBS, int bs
  * block past n are never used, whatever they hold.
  *
  * Work split: every (sequence, KV head) context is a stream of 16-token
- * boxes; the concatenated streams are cut into equal slices over a
- * persistent grid (eight worker warps per CTA, one CTA per SM), and a second
- * kernel merges, by log-sum-exp, the pieces of contexts that straddle
- * workers.  Both kernels run on `stream`.
+ * boxes; the concatenated streams are cut into equal slices, one per worker
+ * warp of a persistent grid (two CTAs of four workers per SM, or one CTA of
+ * eight workers per SM where the smaller CTAs do not fit twice in shared
+ * memory: large B, or G = 8 at D = 128), and a second kernel merges, by
+ * log-sum-exp, the pieces of contexts that straddle workers.  Both kernels
+ * run on `stream`.
  *
  *   q             bf16 [B, Hq, D]
  *   k_cache,
@@ -135,7 +141,8 @@ size_t pkv_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int MBS, int bs
  *                 pkv_decode_workspace_bytes(B, Hq, Hkv, D, MBS, bs, max_ctas)
  *                 bytes; contents on entry do not matter; it is overwritten,
  *                 so calls that may overlap need separate workspaces
- *   max_ctas      0 = as many CTAs as the device holds at once (up to 256);
+ *   max_ctas      0 = as many CTAs as the device holds at once (at most
+ *                 2048 worker warps in all);
  *                 k >= 1 = at most k CTAs (moves where contexts are split;
  *                 results agree within rounding)
  *   B >= 0, Hq % Hkv == 0, Hq/Hkv in {1, 2, 4, 8}, D in {64, 128},
@@ -224,10 +231,16 @@ pkv_status pkv_store_kvcache_fp8(const void *k, const void *v, void *k_cache, vo
  *
  * Same arguments, workspace (pkv_decode_workspace_bytes with the same
  * sizes) and results, reading K = code_value * k_scale and V = code_value *
- * v_scale.  The contractions run on the tensor cores in f16 with fp32
- * accumulation (E4M3 values are exact in f16; q is rounded to f16, which is
- * exact for |q| in [2^-14, 65504] with at most 11 significant bits, i.e. any
- * bf16 in that range), P in f16, output rounded to bf16.
+ * v_scale.  The contractions run on the tensor cores with fp32 accumulation:
+ *   - scores on the E4M3 path, K as the raw cache codes and q split per head
+ *     into two E4M3 parts under a power-of-two scale sq,
+ *     q = sq * (hi + lo / 16), which is exact for every bf16 element of
+ *     magnitude >= max|q| * 2^-14 (smaller elements are within
+ *     max|q| * 2^-21);
+ *   - P.V in f16: V codes converted to f16 (exact), P rounded to f16;
+ *   - output rounded to bf16.
+ * Three CTAs of four workers run per SM (one CTA of eight where they do not
+ * fit).
  */
 pkv_status pkv_paged_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
                                      const int32_t *block_tables, int MBS,
@@ -247,21 +260,25 @@ pkv_status pkv_paged_attn_decode_fp8(const void *q, const void *k_cache, const v
  * memory pool, or a runtime that only owns the step's input and output
  * buffers.  This call computes exactly what pkv_paged_attn_decode computes
  * (same arguments and results, within rounding) but keeps its scratch in a
- * fixed device array of PKV_NOALLOC_SCRATCH_BYTES inside the library, which
- * every GPU that loads the library's device code holds until the process
- * exits.  It allocates nothing.  The grid is capped so the scratch fits;
- * sizes that do not fit even one CTA (huge B with large G and D) return
- * PKV_ERR_WORKSPACE with a message, and pkv_paged_attn_decode with a
- * caller workspace remains available for them.
+ * fixed device array of PKV_NOALLOC_SCRATCH_BYTES (16 MiB) inside the
+ * library, which every GPU that loads the library's device code holds until
+ * the process exits.  It allocates nothing.  The decode grid is the one
+ * pkv_paged_attn_decode launches with max_ctas = 0 whenever that grid's
+ * partial results fit the array, which holds for every supported size on a
+ * 152-SM GB300; otherwise the grid is capped so they fit (results then agree
+ * within rounding, as for any max_ctas).  Every supported size fits at least
+ * one CTA, so the call never fails for lack of scratch.
  *
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it: make that
- * first call before any CUDA stream capture.  All calls share the one array
- * and it keeps the last call's contents (nothing in it needs to start at
- * zero).  Calls that overlap on the GPU race on it: serialise them (one
- * stream per device, or events between streams).
+ * (cudaGetSymbolAddress, with that device current) and caches it with the id
+ * of the device's current context; a call on a new context (after
+ * cudaDeviceReset, for instance) looks it up again.  Make the first call on a
+ * device before any CUDA stream capture.  All calls share the one array and
+ * it keeps the last call's contents (nothing in it needs to start at zero).
+ * Calls that overlap on the GPU race on it: serialise them (one stream per
+ * device, or events between streams).
  */
-#define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 pkv_status pkv_paged_attn_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                          const int32_t *block_tables, int MBS,

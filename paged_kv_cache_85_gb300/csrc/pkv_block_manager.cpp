@@ -3,7 +3,6 @@
 #include "pkv_block_manager.h"
 
 #include <cstring>
-#include <deque>
 #include <unordered_map>
 #include <vector>
 
@@ -42,23 +41,72 @@ struct Sequence {
     std::vector<int32_t> table;     // block ids, logical order
 };
 
+// FIFO pool of free block ids as a doubly linked list threaded through
+// per-block links: push at the back, pop at the front, and removal of any
+// given id (a prefix-cache hit on a freed block) all take O(1).
+class FreeList {
+  public:
+    void reset(int32_t n)
+    {
+        prev_.assign((size_t)n, -1);
+        next_.assign((size_t)n, -1);
+        in_.assign((size_t)n, 0);
+        head_ = tail_ = -1;
+        size_ = 0;
+    }
+    int64_t size() const { return size_; }
+    bool empty() const { return size_ == 0; }
+    int32_t front() const { return head_; }
+    void push_back(int32_t id)
+    {
+        prev_[id] = tail_;
+        next_[id] = -1;
+        if (tail_ >= 0)
+            next_[tail_] = id;
+        else
+            head_ = id;
+        tail_ = id;
+        in_[id] = 1;
+        size_++;
+    }
+    void remove(int32_t id)
+    {
+        if (!in_[id])
+            return;
+        const int32_t p = prev_[id], n = next_[id];
+        if (p >= 0)
+            next_[p] = n;
+        else
+            head_ = n;
+        if (n >= 0)
+            prev_[n] = p;
+        else
+            tail_ = p;
+        in_[id] = 0;
+        size_--;
+    }
+    void pop_front() { remove(head_); }
+
+  private:
+    std::vector<int32_t> prev_, next_;
+    std::vector<uint8_t> in_;
+    int32_t head_ = -1, tail_ = -1;
+    int64_t size_ = 0;
+};
+
 } // namespace
 
 struct pkv_block_manager {
     int block_size = 0;
     std::vector<Block> blocks;
-    std::deque<int32_t> free_ids;
+    FreeList free_ids;
     std::unordered_map<uint64_t, int32_t> hash_to_block;
     std::unordered_map<int64_t, Sequence> seqs;
 
     // Take a specific free block out of the pool and hand it out (ref 1).
     void take(int32_t id, bool reset_contents)
     {
-        for (auto it = free_ids.begin(); it != free_ids.end(); ++it)
-            if (*it == id) {
-                free_ids.erase(it);
-                break;
-            }
+        free_ids.remove(id);
         Block &blk = blocks[id];
         blk.ref_count = 1;
         if (reset_contents) {
@@ -121,6 +169,7 @@ pkv_status pkv_bm_create(int64_t num_blocks, int block_size, pkv_block_manager *
     auto *bm = new pkv_block_manager();
     bm->block_size = block_size;
     bm->blocks.resize((size_t)num_blocks);
+    bm->free_ids.reset((int32_t)num_blocks);
     for (int64_t i = 0; i < num_blocks; i++)
         bm->free_ids.push_back((int32_t)i);
     *out = bm;

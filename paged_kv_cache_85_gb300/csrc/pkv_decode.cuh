@@ -13,8 +13,11 @@
 //    every K/V byte is read from HBM once.  The streams are concatenated
 //    (KV-head-major); each head's region is cut into equal contiguous
 //    slices, one per worker, so the workers of different heads read the
-//    same token rows at the same time; a worker is one consumer warp, and a
-//    persistent grid of CTAs with eight workers each fills the 152 SMs.
+//    same token rows at the same time; a worker is one consumer warp.  A
+//    persistent grid fills the SMs: two CTAs of four workers (plus a
+//    producer warp) per SM for bf16 caches, three for FP8 caches, and one
+//    CTA of eight workers per SM where two smaller CTAs do not fit in shared
+//    memory (large B, or G = 8 at D = 128).
 //    Every worker therefore moves the same number of bytes (+-1 box), and a
 //    stream is split only where a slice boundary falls into it.  Each CTA
 //    rebuilds the per-sequence box prefix sums from context_lens in shared

@@ -136,3 +136,15 @@ def test_prefill_argument_errors_need_no_gpu(cuda_lib_path):
     # nothing to do: no launch, no device needed
     assert f(None, None, None, None, 4, None, None, 0, 0, 0, 4, 4, 64, 8, 16, 1.0, None, None, None) == 0
     assert f(None, None, None, None, 4, None, None, 2, 10, 5, 4, 4, 64, 8, 16, 1.0, None, None, None) == 1  # null
+
+
+def test_selftest_rejects_bad_limits_on_the_host(cuda_lib_path):
+    """The bounded-wait self-test refuses limits outside (0, 0.1 s] and a
+    missing err_flag before any launch (no GPU needed)."""
+    lib = ctypes.CDLL(cuda_lib_path)
+    f = lib.pkv_selftest_bounded_wait
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(0, 0, ctypes.c_void_p(16), None, None) == 1
+    assert f(200_000_000, 0, ctypes.c_void_p(16), None, None) == 1
+    assert f(1000, 0, None, None, None) == 1

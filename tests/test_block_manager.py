@@ -185,3 +185,52 @@ def test_append_batch_is_all_or_nothing_and_matches_single_appends():
     with pytest.raises(PkvError):
         tight.append_batch([0, 1], [1, 1])
     assert tight.seq_len(0) == 4 and tight.seq_len(1) == 8
+
+
+def test_prefix_hits_on_freed_blocks_scale_to_a_large_cache():
+    """A prefix-cache hit on a freed block takes it out of the middle of the
+    free pool; with ~100k blocks that must not cost a scan of the pool per
+    hit.  500 sequences of 3000 tokens fill ~94k blocks of 16 tokens, are
+    released (their full blocks stay cached in the pool), then come back:
+    every full block is a hit on a freed block."""
+    import time
+
+    bs, n_seq, n_tok = 16, 500, 3000
+    bm = BlockManager(num_blocks=100_000, block_size=bs)
+    rng = np.random.default_rng(40)
+    prompts = [rng.integers(0, 50_000, size=n_tok) for _ in range(n_seq)]
+    first = []
+    for s, p in enumerate(prompts):
+        assert bm.allocate(s, p) == 0
+        first.append(list(bm.block_table(s)))
+    for s in range(n_seq):
+        bm.deallocate(s)
+    assert bm.num_free_blocks == 100_000
+    t0 = time.perf_counter()
+    for s, p in enumerate(prompts):
+        assert bm.allocate(1000 + s, p) == (n_tok // bs) * bs  # every full block cached
+    dt = time.perf_counter() - t0
+    for s in range(n_seq):
+        # the full blocks come back as they were; the partial last block is fresh
+        assert list(bm.block_table(1000 + s))[: n_tok // bs] == first[s][: n_tok // bs]
+    assert bm.num_free_blocks == 100_000 - n_seq * -(-n_tok // bs)
+    assert dt < 5.0, f"{dt:.2f} s for {n_seq * (n_tok // bs)} hits on freed blocks"
+
+
+def test_free_pool_order_after_hits_matches_the_restatement():
+    """Blocks taken out of the middle of the pool by cache hits leave the rest
+    in FIFO order: the next fresh allocations agree with the Python
+    restatement block for block."""
+    bs = 4
+    bm, ref = BlockManager(num_blocks=64, block_size=bs), RefBlockManager(64, bs)
+    rng = np.random.default_rng(41)
+    prompts = [rng.integers(0, 100, size=int(rng.integers(5, 30))) for _ in range(6)]
+    for s, p in enumerate(prompts):
+        assert bm.allocate(s, p) == ref.allocate(s, p)
+    for s in (1, 3, 4):
+        bm.deallocate(s)
+        ref.deallocate(s)
+    for s, p in [(10, prompts[3]), (11, rng.integers(0, 100, size=17)), (12, prompts[1][:9])]:
+        assert bm.allocate(s, p) == ref.allocate(s, p)
+        assert list(bm.block_table(s)) == ref.seqs[s][1]
+    assert bm.num_free_blocks == len(ref.free)

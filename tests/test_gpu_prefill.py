@@ -2,9 +2,10 @@
 
 The step is store_kvcache (bit-exact over the whole cache) then
 paged_prefill.  Attention must match the fp64 oracle to max-abs <= 1e-2 and
-mean-abs <= 1e-3 (bf16 in and out), over every output of the small cases and
-over sampled (token row, head) pairs of the 16k-token steps; every output of
-the large steps must be finite.
+mean-abs <= 1e-3 (bf16 in and out) over every output of every step, the
+16k-token steps included: the oracle runs all their (token row, head) pairs,
+split over the host's cores (each pair is computed on its own, so the split
+changes no bit).
 """
 
 import numpy as np
@@ -76,44 +77,19 @@ def compare(got, ref, what=""):
     return float(err.max()), float(err.mean())
 
 
-def sample_pairs(w, rng, per_seq=48):
-    """(row, head) pairs: every sequence's first and last tokens, tokens on
-    both sides of the kernel's query-tile boundaries (128 (token, head) rows,
-    so 128 / G tokens per tile), and random tokens; random heads."""
-    tpc = 128 // w.G
-    rows = []
-    for b in range(w.B):
-        ql = int(w.q_lens[b])
-        toks = {0, ql - 1, ql // 2}
-        for k in range(1, ql // tpc + 1):
-            toks.update({k * tpc - 1, min(k * tpc, ql - 1)})
-        toks.update(rng.integers(0, ql, size=per_seq).tolist())
-        rows.extend(int(w.cu_seqlens_q[b]) + t for t in sorted(toks) if 0 <= t < ql)
-    heads = rng.integers(0, w.Hq, size=len(rows))
-    pairs = np.stack([np.array(rows), heads], 1).astype(np.int32)
-    # a few rows with every head
-    for r in rng.choice(len(rows), size=min(8, len(rows)), replace=False):
-        pairs = np.concatenate([pairs, np.stack([np.full(w.Hq, rows[r]), np.arange(w.Hq)], 1)
-                                .astype(np.int32)])
-    return pairs
-
-
 _cache = {}
 
 
 def config(idx):
+    """Workload idx with its stored caches and the oracle's full [Tq, Hq, D]
+    output (every row and head)."""
     if idx not in _cache:
         _cache.clear()
         w = wl.prefill_config_workload(idx)
         kc, vc = stored(w)
-        if idx == 0:
-            ref, pairs = oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q,
-                                              w.cu_seqlens_k, w.scale), None
-        else:
-            pairs = sample_pairs(w, np.random.default_rng(idx))
-            ref = oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q,
-                                       w.cu_seqlens_k, w.scale, pairs=pairs)
-        _cache[idx] = (w, kc, vc, ref, pairs)
+        ref = oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k,
+                                   w.scale, threads=oracle.host_cores())
+        _cache[idx] = (w, kc, vc, ref, None)
     return _cache[idx]
 
 
@@ -128,10 +104,8 @@ def test_config_store_bitexact_and_prefill_parity(pkv, idx):
     np.testing.assert_array_equal(bits_host(d["v_cache"]), vc)
     o = bits_host(out)
     assert np.isfinite(wl.bf16_bits_to_f32(o)).all()
-    if pairs is None:
-        compare(o, ref, w.name)
-    else:
-        compare(o[pairs[:, 0], pairs[:, 1]], ref, w.name)
+    assert ref.shape == o.shape  # every output of the step
+    compare(o, ref, w.name)
 
 
 def _random(rng, G, D, bs, q_lens, cached, NB=None, Hkv=2, poison=False):
