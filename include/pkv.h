@@ -72,6 +72,7 @@ typedef enum pkv_status {
 #define PKV_FLAG_BAD_BLOCK 0x2       /* a needed block_tables entry outside [0, NB) */
 #define PKV_FLAG_BAD_CONTEXT_LEN 0x4 /* context_lens[b] < 0 or > MBS*bs (clamped) */
 #define PKV_FLAG_TIMEOUT 0x8         /* an internal pipeline wait gave up (a bug) */
+#define PKV_FLAG_V_RANGE 0x10        /* paged_prefill: a V value beyond f16's range was clamped */
 
 /*
  * pkv_store_kvcache - write the step's new K/V rows into the paged cache.

@@ -38,12 +38,14 @@ __all__ = [
     "FLAG_BAD_BLOCK",
     "FLAG_BAD_CONTEXT_LEN",
     "FLAG_TIMEOUT",
+    "FLAG_V_RANGE",
 ]
 
 FLAG_BAD_SLOT = 0x1
 FLAG_BAD_BLOCK = 0x2
 FLAG_BAD_CONTEXT_LEN = 0x4
 FLAG_TIMEOUT = 0x8
+FLAG_V_RANGE = 0x10  # paged_prefill: a V value beyond f16's range was clamped
 
 _STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
            3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA"}

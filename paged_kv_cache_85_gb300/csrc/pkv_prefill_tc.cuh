@@ -1,38 +1,50 @@
 // Paged prefill attention on the 5th-generation tensor cores (tcgen05/TMEM).
 //
-// Same operation as paged_prefill_kernel (MinivLLM guide §4.5 prepare_prefill;
-// causal: new token i of a sequence sits at position k_len - q_len + i and
-// attends to positions 0 .. that one, K/V read through the block table).
+// What it computes (MinivLLM guide §4.5 prepare_prefill): the new tokens of
+// all sequences are flattened; new token i of a sequence sits at position
+// k_len - q_len + i and attends, causally, to positions 0 .. that one, K/V
+// read through the sequence's block table.
 //
 // Persistent CTAs, two per SM (so one CTA's softmax overlaps the other's
 // MMAs), each walking a list of work items: an item is a tile of 128 (token,
 // head-in-group) rows of one sequence and KV head.  Items are ranked longest
 // first and dealt to the CTAs back and forth (round k: CTA c takes position
 // k nC + c, or k nC + nC - 1 - c for odd k).  The producer publishes each item
-// to the other warps through a two-slot buffer; ring, S-buffer and P.V
-// barrier phases run on over a CTA's items, so an item's Q and first K tiles
-// load, and its first S runs, while the previous item drains.  Warps:
-//   0..3  softmax: thread t owns row t (TMEM lane t) -- no shuffles
-//   4     producer: finds the next item, TMA of its Q tile, then 64-key K and V tiles (four
-//         16-token boxes each, resolved through the block table) into two
-//         separate 2-stage rings, lanes 0-3 for K and 4-7 for V: a K tile is
-//         released as soon as its S MMA completes, so the next K tiles load
-//         while the softmax runs, and V only has to arrive by its P.V
+// to the other warps through a two-slot buffer; ring, S, P and P.V barrier
+// phases run on over a CTA's items, so an item's Q and first K tiles load,
+// and its first S runs, while the previous item drains.  Warps:
+//   0..3  softmax: thread t owns row t (TMEM lane t) -- no shuffles.  Per
+//         64-key tile: load S from TMEM and hand the S buffer back at once,
+//         exponentiate, write P (f16) into one of two P buffers, and convert
+//         the tile's V rows in shared memory from bf16 to f16 in place
+//         (zeroing rows past k_len or of unloaded boxes)
+//   4     producer: finds the next item, TMA of its Q tile, then 64-key K and
+//         V tiles (four 16-token boxes each, resolved through the block
+//         table) into two separate 2-stage rings: a K tile is released as
+//         soon as its S MMA completes, so the next K tiles load while the
+//         softmax runs, and V only has to arrive by its P.V
 //   5     MMA: allocates 256 TMEM columns; one lane issues
-//           S_j = Q K_j^T    (SS, K-major 128-byte-swizzled operands, M=128
-//                             N=64, into one of two S buffers), and
-//           O  += P_j V_j    (P from TMEM, V MN-major from shared memory,
-//                             N=D), P split into bf16 hi + lo parts.
-// TMEM columns: O in [0, D); S buffers at 128 and 192 (64 f32 columns each);
-// P_j overwrites its S buffer (hi in the first 32 columns, lo in the next 32).
-// An S MMA is issued into a buffer only after the P.V that read the P in it
-// has completed (MMAs are not ordered against each other's TMEM accesses),
-// and an item's first P.V, which overwrites O, only after the previous
-// item's epilogue has read O out.
+//           S_j = Q K_j^T    (SS, bf16, K-major 128-byte-swizzled operands,
+//                             M=128 N=64, into the single S buffer), and
+//           O  += P_j V_j    (TS, f16: P from TMEM, V MN-major from shared
+//                             memory, N=D)
+// TMEM columns: O in [0, D); S at 128 (64 f32 columns); P buffers at 192 and
+// 224 (64 f16 keys = 32 columns each, used by tile parity).  Because P does
+// not live in the S buffer, S_{j+1} is issued as soon as the softmax has
+// loaded S_j, and runs while the softmax works on S_j; the softmax writes
+// P_j only after the P.V that read the same P buffer (P.V_{j-2}) has
+// completed (MMAs are not ordered against each other's TMEM accesses).  An
+// item's first P.V, which overwrites O, waits until the previous item's
+// epilogue has read O out.
+// P.V in f16: P = exp2(...) <= 2^8 is rounded to f16 (11 significant bits, 8x
+// finer than bf16, so no hi + lo split is needed for the output tolerance), and
+// V is converted to f16, exact for every bf16 value of magnitude in
+// [2^-14, 65504]; smaller magnitudes round to f16 subnormals (absolute error
+// <= 2^-25), larger finite values and infinities clamp to +-65504 and set
+// PKV_FLAG_V_RANGE; NaN stays NaN.
 // The running max moves only when a row's tile max exceeds it by more than
 // 2^8 (then that warp rescales its O rows in TMEM after the previous P.V has
-// completed).  V rows past k_len or in unloaded boxes are zeroed in shared
-// memory before P.V (their weight is 0, and 0 * NaN would be NaN).
+// completed).
 #pragma once
 
 #include <cuda.h>
@@ -52,7 +64,9 @@ constexpr int kTcKStages = 2;           // K ring depth
 constexpr int kTcVStages = 2;           // V ring depth
 constexpr int kTcThreads = 6 * 32;
 constexpr uint32_t kTcCols = 256;       // TMEM columns per CTA
-constexpr uint32_t kTcSCol = 128;       // first S buffer column
+constexpr uint32_t kTcSCol = 128;       // the S buffer (64 f32 columns)
+constexpr uint32_t kTcPCol = 192;       // P buffers at 192 and 224 (64 f16 keys each)
+constexpr int kFlagVRange = 0x10;       // PKV_FLAG_V_RANGE (pkv.h)
 
 struct TcSmem {
     size_t q, kv, bars, items, slot, total;
@@ -66,8 +80,8 @@ __host__ __device__ inline TcSmem tc_smem_layout(int D)
     o += (size_t)(D / 64) * kTcRows * 128;
     L.kv = o;  // K stages [D/64][64 keys][128 B], then V stages alike
     o += (size_t)(kTcKStages + kTcVStages) * (D / 64) * kTcKeys * 128;
-    L.bars = o;  // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
-                 // p_full[2], pv_done[2], o_free, item_ready[2], item_free[2], mma_done
+    L.bars = o;  // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full,
+                 // s_free, pv_ready[2], pv_done[2], o_free, item_ready[2], item_free[2], mma_done
     o += 8 * (2 + 2 * kTcKStages + 2 * kTcVStages + 2 + 2 + 2 + 1 + 2 + 2 + 1);
     L.items = o;  // two published work items of 32 bytes
     o += 2 * 32;
@@ -243,9 +257,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     uint64_t *k_empty = k_full + kTcKStages;
     uint64_t *v_full = k_empty + kTcKStages;
     uint64_t *v_empty = v_full + kTcVStages;
-    uint64_t *s_full = v_empty + kTcVStages;       // [2] S_g written, by buffer g & 1
-    uint64_t *p_full = s_full + 2;                 // [2] P_g written over it
-    uint64_t *pv_done = p_full + 2;                // [2] P.V_g completed, by buffer g & 1
+    uint64_t *s_full = v_empty + kTcVStages;       // S_g written (once per tile g)
+    uint64_t *s_free = s_full + 1;                 // S_g loaded by all four softmax warps
+    uint64_t *pv_ready = s_free + 1;               // [2] P_g written and V_g converted, by g & 1
+    uint64_t *pv_done = pv_ready + 2;              // [2] P.V_g completed, by P buffer g & 1
     uint64_t *o_free = pv_done + 2;                // the item's O has been read out
     uint64_t *item_ready = o_free + 1;             // [2] item parameters published
     uint64_t *item_free = item_ready + 2;          // [2] item parameters no longer needed
@@ -270,9 +285,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 4);  // one arrival per softmax warp
         for (int i = 0; i < 2; i++) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&pv_ready[i], 4);
             mbar_init(&pv_done[i], 1);
             mbar_init(&item_ready[i], 1);
             mbar_init(&item_free[i], 5);  // the MMA lane and the four softmax warps
@@ -288,7 +304,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *slot;
-    const uint32_t tO = tmem, tS0 = tmem + kTcSCol;
+    const uint32_t tO = tmem, tS = tmem + kTcSCol, tP0 = tmem + kTcPCol;
     const int nC = (int)gridDim.x;
     const int c = (int)blockIdx.x;
 
@@ -463,38 +479,26 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const uint32_t qa = smem_u32(sQ);
             // a negative scale is applied by negating Q (bit 13 of the descriptor)
             const uint32_t idS = tc::idesc_bf16(kTcRows, kTcKeys, false) | (p.neg_scale ? 1u << 13 : 0u);
-            const uint32_t idO = tc::idesc_bf16(kTcRows, D, true);
-            // S_g into buffer g & 1, once K_g has landed and, for g >= 2,
-            // P.V_{g-2} (which read the P in that buffer) has completed: the
-            // tensor pipe does not order that P.V's TMEM reads before a later
-            // MMA's writes.  pv_done[g & 1] is then at most one phase behind
-            // (P.V_g cannot complete before S_g), so its parity wait is exact.
-            auto issue_s = [&](int g, bool last_of_item) -> bool {
+            const uint32_t idO = tc::idesc_f16(kTcRows, D, true);
+            // S_g into the S buffer (the caller has seen K_g land and, for g >= 1,
+            // the four softmax warps load S_{g-1} out of the buffer)
+            auto issue_s_now = [&](int g, bool last_of_item) {
                 const int s = g % kTcKStages;
-                if (!wait_all(&k_full[s], (g / kTcKStages) & 1))
-                    return false;
-                if (g >= 2) {
-                    if (!wait_all(&pv_done[g & 1], ((g - 2) >> 1) & 1))
-                        return false;
-                    tc::fence_after();
-                }
                 const uint32_t ka = smem_u32(sK + (size_t)s * kTile);
-                const uint32_t dst = tS0 + (uint32_t)(g & 1) * kTcKeys;
                 if (tc::elect_one()) {
 #pragma unroll
                     for (int kq = 0; kq < D / 16; kq++) {
                         const uint32_t off = (uint32_t)(kq >> 2) * kQHalf + (uint32_t)(kq & 3) * 32;
                         const uint32_t offk = (uint32_t)(kq >> 2) * kTileHalf + (uint32_t)(kq & 3) * 32;
-                        tc::mma_ss(dst, tc::smem_desc(qa + off, 16, 1024),
+                        tc::mma_ss(tS, tc::smem_desc(qa + off, 16, 1024),
                                    tc::smem_desc(ka + offk, 16, 1024), idS, kq > 0);
                     }
-                    tc::commit(smem_u32(&s_full[g & 1]));
+                    tc::commit(smem_u32(s_full));
                     tc::commit(smem_u32(&k_empty[s]));
                     if (last_of_item)
                         tc::commit(smem_u32(q_empty));
                 }
                 __syncwarp();
-                return true;
             };
             int g0 = 0;  // tiles of the previous items
             for (int n = 0; ok; n++) {
@@ -506,35 +510,64 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 if (!(ok = wait_all(q_full, n & 1)))
                     break;
                 tc::fence_after();
-                if (!(ok = issue_s(g0, it.nkt == 1)))
-                    break;
-                for (int j = 0; j < it.nkt && ok; j++) {
-                    const int g = g0 + j;
-                    if (j + 1 < it.nkt && !(ok = issue_s(g + 1, j + 2 == it.nkt)))
-                        break;
-                    if (!(ok = wait_all(&p_full[g & 1], (g >> 1) & 1)))
-                        break;
-                    if (!(ok = wait_all(&v_full[g % kTcVStages], (g / kTcVStages) & 1)))
-                        break;
-                    // the first P.V of an item overwrites O: the previous item's
-                    // epilogue must have read it out
-                    if (j == 0 && n >= 1 && !(ok = wait_all(o_free, (n - 1) & 1)))
-                        break;
-                    tc::fence_after();
-                    const int s = g % kTcVStages;
-                    const uint32_t va = smem_u32(sV + (size_t)s * kTile);
-                    const uint32_t pS = tS0 + (uint32_t)(g & 1) * kTcKeys;
-                    if (tc::elect_one()) {
+                // Readiness-driven issue: the warp polls (never blocking) whether
+                // the next P.V and the next S can go and issues P.V first, so V
+                // stages return to the producer as early as possible; S needs its
+                // K tile and the single S buffer back (s_free).  Every parity test
+                // is at most one phase behind: pv_ready for g + 2 follows P_{g+2},
+                // which the softmax writes only after P.V_g has completed; s_free
+                // for g needs S_g, which is issued only after s_free for g - 1.
+                const int gend = g0 + it.nkt;
+                int ns = g0, np = g0;  // next S and next P.V (tile indices of this CTA)
+                uint64_t t_last = global_timer_ns();
+                while (np < gend) {
+                    bool prog = false;
+                    if (np < ns) {
+                        bool rdy = tc::test_wait(smem_u32(&pv_ready[np & 1]), (np >> 1) & 1);
+                        // the first P.V of an item overwrites O: the previous item's
+                        // epilogue must have read it out
+                        if (rdy && np == g0 && n >= 1)
+                            rdy = tc::test_wait(smem_u32(o_free), (n - 1) & 1);
+                        if (__shfl_sync(FULL, rdy, 0)) {
+                            tc::fence_after();
+                            const int s = np % kTcVStages;
+                            const uint32_t va = smem_u32(sV + (size_t)s * kTile);
+                            const uint32_t pP = tP0 + (uint32_t)(np & 1) * (kTcKeys / 2);
+                            if (tc::elect_one()) {
 #pragma unroll
-                        for (int kk = 0; kk < kTcKeys / 16; kk++) {
-                            const uint64_t dv = tc::smem_desc(va + kk * 16 * 128, kTileHalf, 1024);
-                            tc::mma_ts(tO, pS + 8 * kk, dv, idO, (j > 0 || kk > 0) ? 1u : 0u);
-                            tc::mma_ts(tO, pS + 32 + 8 * kk, dv, idO, 1u);
+                                for (int kk = 0; kk < kTcKeys / 16; kk++) {
+                                    const uint64_t dv = tc::smem_desc(va + kk * 16 * 128, kTileHalf, 1024);
+                                    tc::mma_ts(tO, pP + 8 * kk, dv, idO, (np > g0 || kk > 0) ? 1u : 0u);
+                                }
+                                tc::commit(smem_u32(&v_empty[s]));
+                                tc::commit(smem_u32(&pv_done[np & 1]));
+                            }
+                            __syncwarp();
+                            np++;
+                            prog = true;
                         }
-                        tc::commit(smem_u32(&v_empty[s]));
-                        tc::commit(smem_u32(&pv_done[g & 1]));
                     }
-                    __syncwarp();
+                    if (!prog && ns < gend) {
+                        bool rdy = tc::test_wait(smem_u32(&k_full[ns % kTcKStages]),
+                                                 (ns / kTcKStages) & 1);
+                        if (rdy && ns >= 1)
+                            rdy = tc::test_wait(smem_u32(s_free), (ns - 1) & 1);
+                        if (__shfl_sync(FULL, rdy, 0)) {
+                            tc::fence_after();
+                            issue_s_now(ns, ns == gend - 1);
+                            ns++;
+                            prog = true;
+                        }
+                    }
+                    if (prog) {
+                        t_last = global_timer_ns();
+                    } else {
+                        __nanosleep(16);
+                        if (__shfl_sync(FULL, global_timer_ns() - t_last > 2000000000ull, 0)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                 }
                 if (!ok)
                     break;
@@ -570,23 +603,71 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const int32_t *table = p.block_tables + (size_t)it.b * p.MBS;
             const int nkt = it.nkt, k_len = it.k_len;
             float m = -INFINITY, l = 0.f;
+            uint32_t vmax = 0;  // f16 magnitudes of the converted V rows, max per half
+            // V_g in shared memory: bf16 -> f16 in place, rows past k_len or of
+            // unloaded boxes zeroed (their weight is 0, and 0 * NaN would be NaN);
+            // then P.V_g may be issued (P_g was written one tile earlier).  Done
+            // while the warps work on tile g + 1, so V_g has a tile more to land.
+            auto convert_v = [&](int gv, uint32_t vmask_bits, int kb) -> bool {
+                const int sv = gv % kTcVStages;
+                if (!__all_sync(FULL, mbar_wait(&v_full[sv], (gv / kTcVStages) & 1)))
+                    return false;
+                uint4 *vt = reinterpret_cast<uint4 *>(sV + (size_t)sv * kTile);
+                const bool vmask = vmask_bits != 0xFu || kb + kTcKeys > k_len;
+                // every load first, then the conversions, then every store: thread r
+                // owns 16-byte chunks r + 128 u (chunk i: half i / 512, key row
+                // (i / 8) % 64, one of the row's eight column groups)
+                constexpr int NCH = HALVES * kTcKeys * 8 / 128;
+                uint4 w[NCH];
+#pragma unroll
+                for (int u = 0; u < NCH; u++)
+                    w[u] = vt[r + 128 * u];
+#pragma unroll
+                for (int u = 0; u < NCH; u++) {
+                    w[u].x = bf16x2_to_f16x2_sat(w[u].x);
+                    w[u].y = bf16x2_to_f16x2_sat(w[u].y);
+                    w[u].z = bf16x2_to_f16x2_sat(w[u].z);
+                    w[u].w = bf16x2_to_f16x2_sat(w[u].w);
+                }
+                if (vmask) {  // the same for the whole CTA: a tile with rows to clear
+#pragma unroll
+                    for (int u = 0; u < NCH; u++) {
+                        const int kr = ((r + 128 * u) / 8) % kTcKeys;
+                        if (kb + kr >= k_len || !((vmask_bits >> (kr / kBox)) & 1u))
+                            w[u] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < NCH; u++)
+                    vmax = f16x2_absmax(vmax, f16x2_absmax(f16x2_absmax(w[u].x, w[u].y),
+                                                           f16x2_absmax(w[u].z, w[u].w)));
+#pragma unroll
+                for (int u = 0; u < NCH; u++)
+                    vt[r + 128 * u] = w[u];
+                fence_proxy_async_smem();
+                tc::fence_before();  // also orders this warp's tcgen05.st of P_g
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&pv_ready[gv & 1]);
+                return true;
+            };
+            uint32_t prev_mask = 0;
+            int prev_kb = 0;
+            // boxes of a tile the producer loads (block ids in [0, NB)); read from
+            // the table here, not from the producer, whose K stage may already hold
+            // a later tile.  Lanes 0-3 read the entries of the next tile one tile
+            // ahead, so the load's latency is off the softmax's path.
+            auto table_entry = [&](int jt) -> int {
+                const int key0 = jt * kTcKeys + (lane & 3) * kBox;
+                return (lane < 4 && jt < nkt && key0 < k_len) ? __ldg(table + key0 / p.bs) : -1;
+            };
+            int blk_next = table_entry(0);
             for (int j = 0; j < nkt; j++) {
                 const int gt = g0 + j;
-                const uint32_t tS = tS0 + (uint32_t)(gt & 1) * kTcKeys;
-                // boxes of this tile the producer loads (block ids in [0, NB)); read
-                // from the table here, not from the producer, whose K stage may
-                // already hold a later tile
-                uint32_t mask;
-                {
-                    const int key0 = j * kTcKeys + (lane & 3) * kBox;
-                    bool ld = false;
-                    if (lane < 4 && key0 < k_len) {
-                        const int blk = __ldg(table + key0 / p.bs);
-                        ld = blk >= 0 && blk < p.NB;
-                    }
-                    mask = __ballot_sync(FULL, ld) & 0xFu;
-                }
-                ok = __all_sync(FULL, mbar_wait(&s_full[gt & 1], (gt >> 1) & 1));
+                const int blk = blk_next;
+                blk_next = table_entry(j + 1);
+                const uint32_t mask = __ballot_sync(FULL, blk >= 0 && blk < p.NB) & 0xFu;
+                ok = __all_sync(FULL, mbar_wait(s_full, gt & 1));
                 if (!ok)
                     break;
                 tc::fence_after();
@@ -604,13 +685,24 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                         x[32 + i] = __uint_as_float(rb[i]);
                     }
                 }
+                // S is in registers: the MMA warp may issue S_{g+1} into the buffer
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(s_free);
+                if (j > 0 && !(ok = convert_v(gt - 1, prev_mask, prev_kb)))
+                    break;
                 const int key_base = j * kTcKeys;
+                // masked keys: past this row's position (the diagonal tiles) or in
+                // an unloaded box.  Most tiles have none in the whole warp: they
+                // take the paths without any per-key select.
                 const bool masked = mask != 0xFu || key_base + kTcKeys - 1 > pos;
-                if (masked) {
+                const bool any_masked = __any_sync(FULL, masked);
+                if (any_masked) {
+                    const int lim = pos - key_base;  // keys i > lim are in the future
 #pragma unroll
                     for (int i = 0; i < kTcKeys; i++)
-                        if (key_base + i > pos || !((mask >> (i / kBox)) & 1u))
-                            x[i] = -INFINITY;
+                        x[i] = (i > lim || !((mask >> (i / kBox)) & 1u)) ? -INFINITY : x[i];
                 }
                 float mraw;
                 {
@@ -631,8 +723,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     const float alpha = mn == -INFINITY ? 1.f : fast_exp2(m - mn);
                     if (j > 0) {
                         // O holds P_0..P_{j-1} V: rescale once the last P.V completed
-                        // (pv_done of its buffer, at most one phase behind: the next
-                        // P.V in that buffer needs this warp's next P)
+                        // (its pv_ready was arrived above; pv_done of its P buffer is at
+                        // most one phase behind: the buffer's previous P.V was awaited
+                        // before P_{g-1} was written, and its next one needs this
+                        // warp's next P)
                         if (!(ok = __all_sync(FULL, mbar_wait(&pv_done[(gt - 1) & 1],
                                                               ((gt - 1) >> 1) & 1))))
                             break;
@@ -653,47 +747,60 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     m = mn;
                 }
                 const float nmu = m == -INFINITY ? 0.f : -m;
+                uint32_t pk[32];
                 {
-                    uint32_t hi[32], lo[32];
-                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                    // p = exp2(x sl - m), two keys per packed f32x2 FMA and add
+                    const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(nmu, nmu);
+                    float2 ls0 = make_float2(0.f, 0.f), ls1 = ls0;
+                    if (!any_masked) {
 #pragma unroll
-                    for (int i = 0; i < 32; i++) {
-                        float p0 = fast_exp2(fmaf(x[2 * i], sl, nmu));
-                        float p1 = fast_exp2(fmaf(x[2 * i + 1], sl, nmu));
-                        if (masked) {  // exact zeros for masked keys (also when the scale is 0)
-                            p0 = x[2 * i] == -INFINITY ? 0.f : p0;
-                            p1 = x[2 * i + 1] == -INFINITY ? 0.f : p1;
+                        for (int i = 0; i < 32; i++) {
+                            const float2 a = ffma2(make_float2(x[2 * i], x[2 * i + 1]), sl2, nm2);
+                            const float2 e = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                            if (i & 1)
+                                ls1 = fadd2(ls1, e);
+                            else
+                                ls0 = fadd2(ls0, e);
+                            pk[i] = pack_f16x2(e.x, e.y);
                         }
-                        ls[i & 3] += p0 + p1;
-                        hi[i] = pack_bf16x2(p0, p1);
-                        const float2 h = bf16x2_to_float2(hi[i]);
-                        lo[i] = pack_bf16x2(p0 - h.x, p1 - h.y);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) {
+                            float2 a = ffma2(make_float2(x[2 * i], x[2 * i + 1]), sl2, nm2);
+                            // exact zeros for masked keys (also when the scale is 0,
+                            // where -inf * 0 would be NaN): exp2(-inf) = 0
+                            a.x = x[2 * i] == -INFINITY ? -INFINITY : a.x;
+                            a.y = x[2 * i + 1] == -INFINITY ? -INFINITY : a.y;
+                            const float2 e = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                            if (i & 1)
+                                ls1 = fadd2(ls1, e);
+                            else
+                                ls0 = fadd2(ls0, e);
+                            pk[i] = pack_f16x2(e.x, e.y);
+                        }
                     }
-                    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    tc::st32(tS + tl, hi);
-                    tc::st32(tS + tl + 32, lo);
-                    tc::wait_st();
+                    l += (ls0.x + ls0.y) + (ls1.x + ls1.y);
                 }
-                // V rows past k_len or in unloaded boxes: zero them (all four warps)
-                if (mask != 0xFu || key_base + kTcKeys > k_len) {
-                    // after the V copies of this tile have landed
-                    const int sv = gt % kTcVStages;
-                    if (!(ok = __all_sync(FULL, mbar_wait(&v_full[sv], (gt / kTcVStages) & 1))))
+                // P buffer gt & 1 was last read by P.V_{gt-2}: wait for it.  At most
+                // one phase behind: P.V_{gt-4} was awaited before P_{gt-2} was
+                // written, and P.V_gt needs the V conversion of the next step.
+                if (gt >= 2) {
+                    if (!(ok = __all_sync(FULL, mbar_wait(&pv_done[gt & 1], ((gt - 2) >> 1) & 1))))
                         break;
-                    uint8_t *vt = sV + (size_t)sv * kTile;
-                    for (int i2 = r; i2 < HALVES * kTcKeys * 8; i2 += 128) {
-                        const int h = i2 / (kTcKeys * 8), kr = (i2 / 8) % kTcKeys, c8 = i2 % 8;
-                        if (key_base + kr >= k_len || !((mask >> (kr / kBox)) & 1u))
-                            *reinterpret_cast<uint4 *>(vt + h * kTileHalf + kr * 128 + c8 * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
+                    tc::fence_after();
                 }
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&p_full[gt & 1]);
+                tc::st32(tP0 + (uint32_t)(gt & 1) * (kTcKeys / 2) + tl, pk);
+                tc::wait_st();
+                prev_mask = mask;
+                prev_kb = key_base;
             }
+            // the item's last V tile, after which its last P.V may run
+            if (ok)
+                ok = convert_v(g0 + nkt - 1, prev_mask, prev_kb);
+            // a converted V value was clamped to +-65504 (beyond f16's range): bf16
+            // values at or below 65280 convert exactly, so only a clamp gives 0x7bff
+            if (ok && ((vmax & 0x7fffu) >= 0x7bffu || ((vmax >> 16) & 0x7fffu) >= 0x7bffu))
+                flag_error(p.err_flag, kFlagVRange);
             if (!ok)
                 break;
             // the item's last P.V done (its pv_done is at most one phase behind:

@@ -277,6 +277,47 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 
 // ---- math ------------------------------------------------------------------
 // 2^x on the special-function unit (flushes subnormal results to zero).
+// bf16x2 -> f16x2 (round to nearest even; finite values beyond +-65504 and
+// infinities saturate to +-65504, NaN stays NaN).  Each bf16 half widens to
+// fp32 exactly, then one conversion rounds the pair.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t w)
+{
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Per half: a value whose magnitude is max(|a|, |b|) (its sign bit is the xor
+// of the inputs' signs and carries nothing here).
+__device__ __forceinline__ uint32_t f16x2_absmax(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Packed fp32 pairs (sm_100 f32x2 instructions): d = a * b + c and d = a + b,
+// each lane of the pair rounded as its scalar counterpart would be.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)),
+          "l"(*reinterpret_cast<const uint64_t *>(&c)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
 __device__ __forceinline__ float fast_exp2(float x)
 {
     float y;

@@ -172,6 +172,13 @@ def test_long_context_rows_across_many_tiles(pkv):
     compare(bits_host(run_step(pkv, w, to_dev(w))), ref, "long")
 
 
+def f16_rounded(bits):
+    """bf16 bits of V as the kernel's P.V sees it: rounded to f16 (exact for
+    |v| >= 2^-17, where f16 holds every bf16 value), back in bf16 bits."""
+    v = wl.bf16_bits_to_f32(bits).astype(np.float16).astype(np.float32)
+    return wl.f32_to_bf16_bits(v)
+
+
 def test_first_token_of_a_fresh_sequence_returns_its_v_bitexact(pkv):
     rng = np.random.default_rng(511)
     w = _random(rng, 4, 128, 16, [5, 40, 1], [0, 0, 0])
@@ -181,7 +188,49 @@ def test_first_token_of_a_fresh_sequence_returns_its_v_bitexact(pkv):
         r = int(w.cu_seqlens_q[b])
         blk = w.block_tables[b, 0]
         for h in range(w.Hq):
-            np.testing.assert_array_equal(out[r, h], vc[blk, 0, h // w.G])
+            v = vc[blk, 0, h // w.G]
+            np.testing.assert_array_equal(out[r, h], f16_rounded(v))
+            assert np.array_equal(f16_rounded(v), v)  # N(0,1) data: every value exact in f16
+
+
+def test_tiny_v_values_round_to_f16_subnormals(pkv):
+    """V scaled by 2^-20 (magnitudes around 1e-6, below f16's normal range):
+    the output matches the oracle over V rounded to f16, relative to the
+    scale, and differs from the exact oracle by at most 2^-25 per value."""
+    rng = np.random.default_rng(517)
+    w = _random(rng, 2, 128, 16, [3, 40, 70], [16, 0, 32])
+    for name in ("v_cache", "v_new"):
+        x = wl.bf16_bits_to_f32(getattr(w, name)) * np.float32(2.0 ** -20)
+        setattr(w, name, wl.f32_to_bf16_bits(x))
+    kc, vc = stored(w)
+    got = wl.bf16_bits_to_f32(bits_host(run_step(pkv, w, to_dev(w)))).astype(np.float64)
+    ref16 = oracle.paged_prefill(w.q, kc, f16_rounded(vc), w.block_tables, w.cu_seqlens_q,
+                                 w.cu_seqlens_k, w.scale)
+    ref = oracle.paged_prefill(w.q, kc, vc, w.block_tables, w.cu_seqlens_q, w.cu_seqlens_k,
+                               w.scale)
+    err = np.abs(got - ref16) * 2.0 ** 20
+    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
+    assert np.abs(ref16 - ref).max() <= 2.0 ** -25 * (1 + 1e-6)
+
+
+def test_v_beyond_f16_range_is_clamped_and_flagged(pkv):
+    """65280 (the largest bf16 value within f16's range) passes unflagged; a
+    value of 65536 or more in a row that is read sets PKV_FLAG_V_RANGE and
+    the output stays finite."""
+    rng = np.random.default_rng(518)
+    w = _random(rng, 2, 64, 16, [9, 20], [16, 0])
+    b, t = 1, 3  # sequence 1, token 3: read by its own and later queries
+    slot = int(w.slot_mapping[int(w.cu_seqlens_q[b]) + t])
+    for val, flagged in ((65280.0, False), (65536.0, True), (1.0e6, True)):
+        kc, vc = stored(w)
+        vc = vc.copy()
+        vc[slot // w.bs, slot % w.bs, 0, 5] = wl.f32_to_bf16_bits(np.float32([val]))[0]
+        d = to_dev(w)
+        d["k_cache"], d["v_cache"] = bf16_dev(kc), bf16_dev(vc)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = run_step(pkv, w, d, err=err, store=False)
+        assert bool(int(err.item()) & pkv.FLAG_V_RANGE) == flagged, (val, int(err.item()))
+        assert torch.isfinite(out.float()).all()
 
 
 def test_nan_in_unread_slots_changes_nothing(pkv):
