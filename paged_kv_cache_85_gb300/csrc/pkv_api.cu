@@ -596,9 +596,11 @@ pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_c
         (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
         (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
         return fail(PKV_ERR_INVALID_ARG, "paged_prefill: misaligned pointer");
-    const long long tiles = ((long long)max_seqlen_q * G + pkv::kPrefillRows - 1) / pkv::kPrefillRows;
-    if (tiles * Hkv * B > 0x7fffffffLL)
-        return fail(PKV_ERR_UNSUPPORTED, "paged_prefill: query tiles x Hkv x B must be < 2^31");
+    // work items: pairs of adjacent 128-row query tiles of one sequence and KV head
+    const long long pairs =
+        ((long long)max_seqlen_q * G + 2 * pkv::kPrefillRows - 1) / (2 * pkv::kPrefillRows);
+    if (pairs * Hkv * B > 0x7fffffffLL)
+        return fail(PKV_ERR_UNSUPPORTED, "paged_prefill: query tile pairs x Hkv x B must be < 2^31");
 
     DeviceState *st = nullptr;
     pkv_status ps = device_state(&st);
@@ -640,18 +642,15 @@ pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_c
     p.bs = bs;
     p.NB = (int)NB;
     p.max_q = max_seqlen_q;
-    p.X = (int)tiles;
-    p.n_items = (int)(tiles * Hkv * B);
+    p.X = (int)pairs;
+    p.n_items = (int)(pairs * Hkv * B);
     p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
     p.neg_scale = scale < 0.f;
-    // Persistent grid: two CTAs per SM, each walking its share of the work
-    // items.  The kernel is built for two (each holds half the SM's TMEM
-    // columns, half its shared memory at most, and <= 170 registers a
-    // thread).  The occupancy query is not used: it reports one CTA per SM
-    // for this kernel, while the SM runs two.
-    static_assert(pkv::kPrefillThreads * 170 * 2 <= 65536, "two prefill CTAs per SM by registers");
-    const int per_sm = smem + pkv::kSmemReserve <= pkv::kSmemPerSm / 2 ? 2 : 1;
-    long long grid = (long long)st->sms * per_sm;
+    // Persistent grid: one CTA per SM (each holds all of the SM's TMEM
+    // columns, and asks for more than half of its shared memory so that no
+    // second CTA lands beside it), each walking its share of the work items.
+    static_assert(pkv::kPrefillThreads * 186 <= 65536, "prefill registers per thread");
+    long long grid = (long long)st->sms;
     if (grid > p.n_items)
         grid = p.n_items;
     if (grid < 1)

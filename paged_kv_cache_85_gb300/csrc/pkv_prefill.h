@@ -19,8 +19,8 @@ struct PrefillParams {
     long long Tq;
     int B, Hq, Hkv, MBS, bs, NB;
     int max_q;                    // the caller's bound on q_len (sizes the work space)
-    int X;                        // query tiles per sequence at max_q
-    int n_items;                  // work items: X tiles x Hkv heads x B sequences
+    int X;                        // query tile pairs per sequence at max_q
+    int n_items;                  // work items: X tile pairs x Hkv heads x B sequences
     float scale_log2;             // |scale| * log2(e)
     int neg_scale;                // scale < 0: the score MMA negates Q
 };
@@ -30,7 +30,7 @@ cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmq, const CUtensorM
                            cudaStream_t stream);
 const void *prefill_kernel(int D, int G);
 size_t prefill_smem_bytes(int D);
-constexpr int kPrefillRows = 128;  // (token, head) rows per CTA
-constexpr int kPrefillThreads = 6 * 32;
+constexpr int kPrefillRows = 128;  // (token, head) rows per query tile (two tiles per work item)
+constexpr int kPrefillThreads = 11 * 32;
 
 } // namespace pkv

@@ -5,51 +5,50 @@
 // k_len - q_len + i and attends, causally, to positions 0 .. that one, K/V
 // read through the sequence's block table.
 //
-// Persistent CTAs, two per SM (so one CTA's softmax overlaps the other's
-// MMAs), each walking a list of work items: an item is a tile of 128 (token,
-// head-in-group) rows of one sequence and KV head.  Items are ranked longest
-// first and dealt to the CTAs back and forth (round k: CTA c takes position
-// k nC + c, or k nC + nC - 1 - c for odd k).  The producer publishes each item
-// to the other warps through a two-slot buffer; ring, S, P and P.V barrier
-// phases run on over a CTA's items, so an item's Q and first K tiles load,
-// and its first S runs, while the previous item drains.  Warps:
-//   0..3  softmax: thread t owns row t (TMEM lane t) -- no shuffles.  Per
-//         64-key tile: load S from TMEM and hand the S buffer back at once,
-//         exponentiate, write P (f16) into one of two P buffers, and convert
-//         the tile's V rows in shared memory from bf16 to f16 in place
-//         (zeroing rows past k_len or of unloaded boxes)
-//   4     producer: finds the next item, TMA of its Q tile, then 64-key K and
+// One persistent CTA per SM.  A work item is a pair of adjacent query tiles
+// (A and B, 128 (token, head-in-group) rows each) of one sequence and KV
+// head, so every 64-key K/V tile loaded serves 256 query rows: half the load
+// traffic per row of one tile per CTA, which leaves the shared memory for
+// four-stage K and V rings that cover the copies' latency.  Items are ranked
+// longest first and dealt to the CTAs back and forth (round k: CTA c takes
+// position k nC + c, or k nC + nC - 1 - c for odd k); the producer publishes
+// each item through a two-slot buffer, and every ring, S, P and P.V phase
+// runs on over a CTA's items.  Warps:
+//   0..3  softmax of tile A, 4..7 softmax of tile B: thread t of a group owns
+//         row t (TMEM lane t).  Per 64-key tile: load S from TMEM and hand the
+//         S buffer back at once, exponentiate, write P (f16) into one of the
+//         tile's two P buffers, and convert the previous V tile in shared
+//         memory from bf16 to f16 (rows past k_len or of unloaded boxes
+//         zeroed), each group one half of it when both tiles read it
+//   8     producer: finds the next item, TMA of its Q tiles, then 64-key K and
 //         V tiles (four 16-token boxes each, resolved through the block
-//         table) into two separate 2-stage rings: a K tile is released as
-//         soon as its S MMA completes, so the next K tiles load while the
-//         softmax runs, and V only has to arrive by its P.V
-//   5     MMA: allocates 256 TMEM columns; one lane issues
-//           S_j = Q K_j^T    (SS, bf16, K-major 128-byte-swizzled operands,
-//                             M=128 N=64, into the single S buffer), and
-//           O  += P_j V_j    (TS, f16: P from TMEM, V MN-major from shared
-//                             memory, N=D)
-// TMEM columns: O in [0, D); S at 128 (64 f32 columns); P buffers at 192 and
-// 224 (64 f16 keys = 32 columns each, used by tile parity).  Because P does
-// not live in the S buffer, S_{j+1} is issued as soon as the softmax has
-// loaded S_j, and runs while the softmax works on S_j; the softmax writes
-// P_j only after the P.V that read the same P buffer (P.V_{j-2}) has
-// completed (MMAs are not ordered against each other's TMEM accesses).  An
-// item's first P.V, which overwrites O, waits until the previous item's
-// epilogue has read O out.
-// P.V in f16: P = exp2(...) <= 2^8 is rounded to f16 (11 significant bits, 8x
-// finer than bf16, so no hi + lo split is needed for the output tolerance), and
-// V is converted to f16, exact for every bf16 value of magnitude in
-// [2^-14, 65504]; smaller magnitudes round to f16 subnormals (absolute error
-// <= 2^-25), larger finite values and infinities clamp to +-65504 and set
-// PKV_FLAG_V_RANGE; NaN stays NaN.
+//         table) into separate 4-stage rings
+//   9     MMA: allocates all 512 TMEM columns and issues, as the operands
+//         become ready (P.V first, so V stages return early):
+//           S_t = Q_t K_j^T   (SS, bf16, K-major 128-byte-swizzled, M=128 N=64)
+//           O_t += P_t V_j    (TS, f16: P from TMEM, V MN-major, N=D)
+// TMEM columns: O_A [0, D), O_B [128, 128 + D), S_A 256, S_B 320 (64 f32
+// columns each), P buffers at 384 (A) and 448 (B), two of 32 columns each
+// (64 f16 keys).  S_t(j+1) is issued once the group has loaded S_t(j), and
+// runs while it works on S_t(j); the group writes P_t(j) only after the P.V
+// that read the same P buffer (P.V_t(j-2)) has completed (MMAs are not
+// ordered against each other's TMEM accesses); an item's first P.V of a tile
+// waits until that tile's previous epilogue has read O out.
+// P.V in f16: P = exp2(...) <= 2^8 is rounded to f16 (11 significant bits),
+// and V is converted to f16, exact for every bf16 value of magnitude in
+// [2^-14, 65504] (and for any bf16 value >= 2^-17); smaller magnitudes round
+// to f16 subnormals (absolute error <= 2^-25), larger finite values and
+// infinities clamp to +-65504 and set PKV_FLAG_V_RANGE; NaN stays NaN.
 // The running max moves only when a row's tile max exceeds it by more than
-// 2^8 (then that warp rescales its O rows in TMEM after the previous P.V has
+// 2^8 (then that group rescales its O rows in TMEM after the previous P.V has
 // completed).
 #pragma once
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "pkv_kernels.h"
 #include "pkv_prefill.h"
@@ -58,36 +57,48 @@
 
 namespace pkv {
 
-constexpr int kTcRows = 128;            // query rows per CTA (MMA M)
+constexpr int kTcRows = 128;            // query rows per Q tile (MMA M)
 constexpr int kTcKeys = 64;             // keys per K/V tile (MMA N of S)
-constexpr int kTcKStages = 2;           // K ring depth
-constexpr int kTcVStages = 2;           // V ring depth
-constexpr int kTcThreads = 6 * 32;
-constexpr uint32_t kTcCols = 256;       // TMEM columns per CTA
-constexpr uint32_t kTcSCol = 128;       // the S buffer (64 f32 columns)
-constexpr uint32_t kTcPCol = 192;       // P buffers at 192 and 224 (64 f16 keys each)
+constexpr int kTcKStages = 4;           // K ring depth
+constexpr int kTcVStages = 4;           // V ring depth
+constexpr int kTcThreads = kPrefillThreads;  // 8 softmax warps, producer, 2 MMA warps
+constexpr int kTcProducerWarp = 8;
+constexpr int kTcMmaWarp = 9;           // warps 9 and 10 issue the MMAs of tiles A and B
+constexpr uint32_t kTcCols = 512;       // all of the SM's TMEM columns
+constexpr uint32_t kTcSCol = 256;       // S_t at 256 + 64 t (64 f32 columns)
+constexpr uint32_t kTcPCol = 384;       // P_t buffers at 384 + 64 t + 32 b (64 f16 keys)
 constexpr int kFlagVRange = 0x10;       // PKV_FLAG_V_RANGE (pkv.h)
+// More than half an SM's shared memory, so that one CTA (which holds every
+// TMEM column) runs per SM.
+constexpr size_t kTcMinSmem = kSmemPerSm / 2 + 4 * 1024;
 
 struct TcSmem {
     size_t q, kv, bars, items, slot, total;
 };
 
+// Barriers: q_full, q_empty, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+// v_conv[VS], then per Q tile: s_full, s_free, pv_ready[2], pv_done[2], o_free;
+// then item_ready[2], item_free[2], mma_done.
+constexpr int kTcTileBars = 7;
+constexpr int kTcBars = 2 + 2 * kTcKStages + 3 * kTcVStages + 2 * kTcTileBars + 2 + 2 + 1;
+
 __host__ __device__ inline TcSmem tc_smem_layout(int D)
 {
     TcSmem L;
     size_t o = 0;
-    L.q = o;  // [D/64 halves][128 rows][128 B]
-    o += (size_t)(D / 64) * kTcRows * 128;
+    L.q = o;  // [tile][D/64 halves][128 rows][128 B]
+    o += (size_t)2 * (D / 64) * kTcRows * 128;
     L.kv = o;  // K stages [D/64][64 keys][128 B], then V stages alike
     o += (size_t)(kTcKStages + kTcVStages) * (D / 64) * kTcKeys * 128;
-    L.bars = o;  // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full,
-                 // s_free, pv_ready[2], pv_done[2], o_free, item_ready[2], item_free[2], mma_done
-    o += 8 * (2 + 2 * kTcKStages + 2 * kTcVStages + 2 + 2 + 2 + 1 + 2 + 2 + 1);
+    L.bars = o;
+    o += 8 * kTcBars;
     L.items = o;  // two published work items of 32 bytes
     o += 2 * 32;
     L.slot = o;
     o += 16;
     L.total = align_up(o, 16) + 1024;
+    if (L.total < kTcMinSmem)
+        L.total = kTcMinSmem;
     return L;
 }
 
@@ -226,14 +237,15 @@ __device__ __forceinline__ PrefillWork prefill_schedule(const PrefillParams &p, 
     return w;  // not reached: rp < count(lo) - count(lo + 1)
 }
 
-// One query tile's work, as the producer publishes it to the other warps.
+// One item's work, as the producer publishes it to the other warps: a pair of
+// adjacent query tiles of one sequence and KV head.
 struct PrefillItem {
-    int b, kvh, tok0, cq0, q_len, k_len, nkt;  // b < 0: no more work for this CTA
-    int pad;
+    int b, kvh, tok0, cq0, q_len, k_len;  // b < 0: no more work for this CTA
+    int nkt[2];  // key tiles of tile A and tile B (0: tile B is past q_len)
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq,
                             const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv, const PrefillParams p)
@@ -241,6 +253,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     constexpr int TPC = kTcRows / G;                  // query tokens per tile
     constexpr int HALVES = D / 64;
     constexpr uint32_t kQHalf = kTcRows * 128;        // 16 KB
+    constexpr uint32_t kQTile = HALVES * kQHalf;
     constexpr uint32_t kTileHalf = kTcKeys * 128;     // 8 KB
     constexpr uint32_t kTile = HALVES * kTileHalf;    // one K (or V) tile
     constexpr uint32_t kBoxBytes = kBox * D * 2;
@@ -251,52 +264,62 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const TcSmem L = tc_smem_layout(D);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *q_full = bars;                       // Q of the item landed (once per item)
+    uint64_t *q_full = bars;                       // the item's Q tiles landed
     uint64_t *q_empty = q_full + 1;                // the item's last S completed: Q may be replaced
     uint64_t *k_full = q_empty + 1;
-    uint64_t *k_empty = k_full + kTcKStages;
+    uint64_t *k_empty = k_full + kTcKStages;       // both tiles' S of the K tile completed
     uint64_t *v_full = k_empty + kTcKStages;
-    uint64_t *v_empty = v_full + kTcVStages;
-    uint64_t *s_full = v_empty + kTcVStages;       // S_g written (once per tile g)
-    uint64_t *s_free = s_full + 1;                 // S_g loaded by all four softmax warps
-    uint64_t *pv_ready = s_free + 1;               // [2] P_g written and V_g converted, by g & 1
-    uint64_t *pv_done = pv_ready + 2;              // [2] P.V_g completed, by P buffer g & 1
-    uint64_t *o_free = pv_done + 2;                // the item's O has been read out
-    uint64_t *item_ready = o_free + 1;             // [2] item parameters published
+    uint64_t *v_empty = v_full + kTcVStages;       // both tiles' P.V of the V tile completed
+    uint64_t *v_conv = v_empty + kTcVStages;       // the V tile converted to f16 (8 warp shares)
+    uint64_t *tbar = v_conv + kTcVStages;          // per Q tile: kTcTileBars barriers
+    uint64_t *item_ready = tbar + 2 * kTcTileBars; // [2] item parameters published
     uint64_t *item_free = item_ready + 2;          // [2] item parameters no longer needed
     uint64_t *mma_done = item_free + 2;            // every MMA of the CTA completed
+    // per Q tile t: s_full (S_t written), s_free (S_t loaded by the tile's four
+    // softmax warps), pv_ready[2] (P_t written, by P buffer), pv_done[2] (P.V_t
+    // completed, by P buffer), o_free (the tile's O read out by its epilogue)
+    auto s_full = [&](int t) { return tbar + kTcTileBars * t; };
+    auto s_free = [&](int t) { return tbar + kTcTileBars * t + 1; };
+    auto pv_ready = [&](int t, int b) { return tbar + kTcTileBars * t + 2 + b; };
+    auto pv_done = [&](int t, int b) { return tbar + kTcTileBars * t + 4 + b; };
+    auto o_free = [&](int t) { return tbar + kTcTileBars * t + 6; };
     uint32_t *slot = reinterpret_cast<uint32_t *>(smem + L.slot);
     PrefillItem *items = reinterpret_cast<PrefillItem *>(smem + L.items);  // [2]
-    uint8_t *sQ = smem + L.q;
+    uint8_t *sQ = smem + L.q;                                          // [2] Q tiles
     uint8_t *sK = smem + L.kv;                                         // kTcKStages K tiles
-    uint8_t *sV = sK + (size_t)kTcKStages * (D / 64) * kTcKeys * 128;  // kTcVStages V tiles
+    uint8_t *sV = sK + (size_t)kTcKStages * kTile;                     // kTcVStages V tiles
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
     grid_launch_dependents();
-    if (warp == 4 && lane == 0) {
+    if (warp == kTcProducerWarp && lane == 0) {
+        // the Q, K and V stages are released by both MMA warps (one arrival each)
         mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
+        mbar_init(q_empty, 2);
         for (int s = 0; s < kTcKStages; s++) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
+            mbar_init(&k_empty[s], 2);
         }
         for (int s = 0; s < kTcVStages; s++) {
             mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
+            mbar_init(&v_empty[s], 2);
+            mbar_init(&v_conv[s], 8);  // one share per softmax warp
         }
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 4);  // one arrival per softmax warp
+        for (int t = 0; t < 2; t++) {
+            mbar_init(s_full(t), 1);
+            mbar_init(s_free(t), 4);
+            for (int b = 0; b < 2; b++) {
+                mbar_init(pv_ready(t, b), 4);
+                mbar_init(pv_done(t, b), 1);
+            }
+            mbar_init(o_free(t), 4);
+        }
         for (int i = 0; i < 2; i++) {
-            mbar_init(&pv_ready[i], 4);
-            mbar_init(&pv_done[i], 1);
             mbar_init(&item_ready[i], 1);
-            mbar_init(&item_free[i], 5);  // the MMA lane and the four softmax warps
+            mbar_init(&item_free[i], 10);  // the two MMA warps and the eight softmax warps
         }
-        mbar_init(o_free, 4);
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 2);
         fence_mbarrier_init();
-    } else if (warp == 5) {
+    } else if (warp == kTcMmaWarp) {
         tc::alloc(smem_u32(slot), kTcCols);
         tc::relinquish();
     }
@@ -304,18 +327,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *slot;
-    const uint32_t tO = tmem, tS = tmem + kTcSCol, tP0 = tmem + kTcPCol;
     const int nC = (int)gridDim.x;
     const int c = (int)blockIdx.x;
 
-    if (warp == 4) {
+    if (warp == kTcProducerWarp) {
         // ------------------------------------------------------------ producer
         // Walks this CTA's items: round k takes position k nC + c (k even) or
-        // k nC + nC - 1 - c (k odd), so the longest-first order is dealt out
-        // back and forth over the CTAs.  For each item: publish it, load Q once
-        // the previous item's last S has read the old Q, then its 64-key K and
-        // V tiles through the two rings (tile counters gk, gv run over all of
-        // this CTA's items).
+        // k nC + nC - 1 - c (k odd).  For each item: publish it, load its Q
+        // tiles once the previous item's last S has read the old ones, then
+        // its 64-key K and V tiles through the two rings (tile counters gk, gv
+        // run over all of this CTA's items).
         if (lane == 0) {
             prefetch_tensormap(&tmq);
             prefetch_tensormap(&tmk);
@@ -328,13 +349,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         int k = 0;               // walk rounds
         for (;;) {
             // ---- the next item with work, or the end
-            PrefillItem it{-1, 0, 0, 0, 0, 0, 0, 0};
+            PrefillItem it{-1, 0, 0, 0, 0, 0, {0, 0}};
             for (; ok; k++) {
                 const long long pos = (long long)k * nC + ((k & 1) ? nC - 1 - c : c);
                 if (pos >= p.n_items)
                     break;
-                const PrefillWork w = p.B <= 32 ? prefill_schedule<TPC, 1>(p, lane, (int)pos)
-                                                : prefill_schedule<TPC, kSchedChunks>(p, lane, (int)pos);
+                const PrefillWork w = p.B <= 32 ? prefill_schedule<2 * TPC, 1>(p, lane, (int)pos)
+                                                : prefill_schedule<2 * TPC, kSchedChunks>(p, lane, (int)pos);
                 int cq0 = w.cq0, cq1 = w.cq1, ck0 = w.ck0, ck1 = w.ck1;
                 if (w.b >= 0 && cq0 == kNotLoaded) {
                     cq0 = __ldg(p.cu_q + w.b);
@@ -345,7 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 const bool sane = w.b >= 0 && prefill_seq_sane(p, cq0, cq1, ck0, ck1);
                 if (w.b >= 0 && !sane && lane == 0)
                     flag_error(p.err_flag, 0x4 /* PKV_FLAG_BAD_CONTEXT_LEN */);
-                const int tok0 = w.tile * TPC;
+                const int tok0 = w.tile * 2 * TPC;
                 if (sane && tok0 < cq1 - cq0) {
                     it.b = w.b;
                     it.kvh = w.kvh;
@@ -353,8 +374,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     it.cq0 = cq0;
                     it.q_len = cq1 - cq0;
                     it.k_len = ck1 - ck0;
-                    const int last_pos = (it.k_len - it.q_len) + min(it.q_len, tok0 + TPC) - 1;
-                    it.nkt = last_pos / kTcKeys + 1;
+                    const int base = it.k_len - it.q_len;
+                    it.nkt[0] = (base + min(it.q_len, tok0 + TPC) - 1) / kTcKeys + 1;
+                    it.nkt[1] = tok0 + TPC < it.q_len
+                                    ? (base + min(it.q_len, tok0 + 2 * TPC) - 1) / kTcKeys + 1
+                                    : 0;
                     k++;
                     break;
                 }
@@ -379,14 +403,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 mbar_arrive(&item_ready[sl]);
             if (it.b < 0)
                 break;
-            // ---- Q, after the previous item's last S
+            // ---- Q tiles, after the previous item's last S
             if (n >= 1 && !(ok = __all_sync(FULL, mbar_wait(q_empty, (n - 1) & 1))))
                 break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(q_full, HALVES * kQHalf);
+                const int nq = it.nkt[1] > 0 ? 2 : 1;
+                mbar_arrive_expect_tx(q_full, (uint32_t)nq * HALVES * kQHalf);
+                for (int t = 0; t < nq; t++)
 #pragma unroll
-                for (int h = 0; h < HALVES; h++)
-                    tma_load_4d(sQ + h * kQHalf, &tmq, 0, h, it.kvh * G, it.cq0 + it.tok0, q_full);
+                    for (int h = 0; h < HALVES; h++)
+                        tma_load_4d(sQ + t * kQTile + h * kQHalf, &tmq, 0, h, it.kvh * G,
+                                    it.cq0 + it.tok0 + t * TPC, q_full);
             }
             n++;
             // ---- K and V tiles.  One converged loop serves both rings: it
@@ -394,21 +421,50 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             // V stage are free and issues whichever tile can go; lanes 0-3
             // resolve and copy one 16-token box each.  K runs ahead of V by up
             // to its ring depth.
+            const int nkt = max(it.nkt[0], it.nkt[1]);
             const int32_t *table = p.block_tables + (size_t)it.b * p.MBS;
+            // Lanes 0-3 resolve one 16-token box each.  A tile's block-table
+            // entries are read once, one K tile ahead of its copy (so the load's
+            // latency is off the producer's path), and kept for the V copy of the
+            // same tile (V lags K by at most the ring depth, four tiles).
+            auto entry = [&](int j) -> int {
+                const int key0 = j * kTcKeys + lane * kBox;
+                return (lane < kTcKeys / kBox && j < nkt && key0 < it.k_len) ? __ldg(table + key0 / p.bs) : -1;
+            };
+            int blk_next = entry(0);
+            int row0 = -1, row1 = -1, row2 = -1, row3 = -1;  // box rows of tiles j % 4 (-1: not loaded)
+            auto put_row = [&](int j, int v) {
+                const int q = j & 3;
+                row0 = q == 0 ? v : row0;
+                row1 = q == 1 ? v : row1;
+                row2 = q == 2 ? v : row2;
+                row3 = q == 3 ? v : row3;
+            };
+            auto get_row = [&](int j) {
+                const int q = j & 3;
+                return q == 0 ? row0 : (q == 1 ? row1 : (q == 2 ? row2 : row3));
+            };
+            static_assert(kTcVStages <= 4 && kTcKStages <= 4, "V lags K by at most four tiles");
             auto issue = [&](int j, int g, bool is_k) {
                 uint64_t *fb = is_k ? k_full : v_full;
                 const int nst = is_k ? kTcKStages : kTcVStages;
                 const int s = g % nst;
-                const int key0 = j * kTcKeys + lane * kBox;
-                bool loaded = false;
-                int row = 0;
-                if (lane < kTcKeys / kBox && key0 < it.k_len) {
-                    const int blk = __ldg(table + key0 / p.bs);
-                    loaded = blk >= 0 && blk < p.NB;
-                    if (!loaded && is_k)
-                        flag_error(p.err_flag, 0x2 /* PKV_FLAG_BAD_BLOCK */);
-                    row = blk * p.bs + key0 % p.bs;
+                int row = -1;
+                if (is_k) {
+                    const int blk = blk_next;
+                    blk_next = entry(j + 1);
+                    const int key0 = j * kTcKeys + lane * kBox;
+                    if (lane < kTcKeys / kBox && key0 < it.k_len) {
+                        if (blk >= 0 && blk < p.NB)
+                            row = blk * p.bs + key0 % p.bs;
+                        else
+                            flag_error(p.err_flag, 0x2 /* PKV_FLAG_BAD_BLOCK */);
+                    }
+                    put_row(j, row);
+                } else {
+                    row = get_row(j);
                 }
+                const bool loaded = row >= 0;
                 const uint32_t mask = __ballot_sync(FULL, loaded);
                 if (lane == 0)
                     mbar_arrive_expect_tx(&fb[s], (uint32_t)__popc(mask) * kBoxBytes);
@@ -422,10 +478,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 }
             };
             int jk = 0, jv = 0;
-            uint64_t t_last = global_timer_ns();
-            while (jk < it.nkt || jv < it.nkt) {
+            uint64_t t_last = sm_clock();
+            while (jk < nkt || jv < nkt) {
                 bool prog = false;
-                if (jk < it.nkt) {
+                // K at most four tiles ahead of the V copies (the kept box rows)
+                if (jk < nkt && jk - jv < 4) {
                     const bool free_k = tc::test_wait(smem_u32(&k_empty[gk % kTcKStages]),
                                                       ((gk / kTcKStages) & 1) ^ 1);
                     if (__shfl_sync(FULL, free_k, 0)) {
@@ -442,10 +499,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     }
                 }
                 if (prog) {
-                    t_last = global_timer_ns();
+                    t_last = sm_clock();
                 } else {
                     __nanosleep(32);
-                    if (__shfl_sync(FULL, global_timer_ns() - t_last > 2000000000ull, 0)) {
+                    if (__shfl_sync(FULL, sm_clock() - t_last > kPollLimitCycles, 0)) {
                         ok = false;
                         break;
                     }
@@ -466,130 +523,137 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 mbar_wait(&v_full[g % kTcVStages], (g / kTcVStages) & 1);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kTcMmaWarp || warp == kTcMmaWarp + 1) {
         // ----------------------------------------------------------------- MMA
-        // The whole warp runs the loop and waits on the barriers; one elected
-        // lane issues the MMAs and their commits (issue from a converged warp
-        // costs fewer cycles per MMA than from a lone lane).
-        {
-            bool ok = true;
-            auto wait_all = [&](uint64_t *bar, uint32_t parity) {
-                return __all_sync(FULL, mbar_wait(bar, parity));
-            };
-            const uint32_t qa = smem_u32(sQ);
-            // a negative scale is applied by negating Q (bit 13 of the descriptor)
-            const uint32_t idS = tc::idesc_bf16(kTcRows, kTcKeys, false) | (p.neg_scale ? 1u << 13 : 0u);
-            const uint32_t idO = tc::idesc_f16(kTcRows, D, true);
-            // S_g into the S buffer (the caller has seen K_g land and, for g >= 1,
-            // the four softmax warps load S_{g-1} out of the buffer)
-            auto issue_s_now = [&](int g, bool last_of_item) {
-                const int s = g % kTcKStages;
-                const uint32_t ka = smem_u32(sK + (size_t)s * kTile);
-                if (tc::elect_one()) {
-#pragma unroll
-                    for (int kq = 0; kq < D / 16; kq++) {
-                        const uint32_t off = (uint32_t)(kq >> 2) * kQHalf + (uint32_t)(kq & 3) * 32;
-                        const uint32_t offk = (uint32_t)(kq >> 2) * kTileHalf + (uint32_t)(kq & 3) * 32;
-                        tc::mma_ss(tS, tc::smem_desc(qa + off, 16, 1024),
-                                   tc::smem_desc(ka + offk, 16, 1024), idS, kq > 0);
-                    }
-                    tc::commit(smem_u32(s_full));
-                    tc::commit(smem_u32(&k_empty[s]));
-                    if (last_of_item)
-                        tc::commit(smem_u32(q_empty));
-                }
-                __syncwarp();
-            };
-            int g0 = 0;  // tiles of the previous items
-            for (int n = 0; ok; n++) {
-                if (!(ok = wait_all(&item_ready[n & 1], (n >> 1) & 1)))
-                    break;
-                const PrefillItem it = items[n & 1];
-                if (it.b < 0)
-                    break;
-                if (!(ok = wait_all(q_full, n & 1)))
-                    break;
-                tc::fence_after();
-                // Readiness-driven issue: the warp polls (never blocking) whether
-                // the next P.V and the next S can go and issues P.V first, so V
-                // stages return to the producer as early as possible; S needs its
-                // K tile and the single S buffer back (s_free).  Every parity test
-                // is at most one phase behind: pv_ready for g + 2 follows P_{g+2},
-                // which the softmax writes only after P.V_g has completed; s_free
-                // for g needs S_g, which is issued only after s_free for g - 1.
-                const int gend = g0 + it.nkt;
-                int ns = g0, np = g0;  // next S and next P.V (tile indices of this CTA)
-                uint64_t t_last = global_timer_ns();
-                while (np < gend) {
-                    bool prog = false;
-                    if (np < ns) {
-                        bool rdy = tc::test_wait(smem_u32(&pv_ready[np & 1]), (np >> 1) & 1);
-                        // the first P.V of an item overwrites O: the previous item's
-                        // epilogue must have read it out
-                        if (rdy && np == g0 && n >= 1)
-                            rdy = tc::test_wait(smem_u32(o_free), (n - 1) & 1);
-                        if (__shfl_sync(FULL, rdy, 0)) {
-                            tc::fence_after();
-                            const int s = np % kTcVStages;
-                            const uint32_t va = smem_u32(sV + (size_t)s * kTile);
-                            const uint32_t pP = tP0 + (uint32_t)(np & 1) * (kTcKeys / 2);
-                            if (tc::elect_one()) {
-#pragma unroll
-                                for (int kk = 0; kk < kTcKeys / 16; kk++) {
-                                    const uint64_t dv = tc::smem_desc(va + kk * 16 * 128, kTileHalf, 1024);
-                                    tc::mma_ts(tO, pP + 8 * kk, dv, idO, (np > g0 || kk > 0) ? 1u : 0u);
-                                }
-                                tc::commit(smem_u32(&v_empty[s]));
-                                tc::commit(smem_u32(&pv_done[np & 1]));
-                            }
-                            __syncwarp();
-                            np++;
-                            prog = true;
-                        }
-                    }
-                    if (!prog && ns < gend) {
-                        bool rdy = tc::test_wait(smem_u32(&k_full[ns % kTcKStages]),
-                                                 (ns / kTcKStages) & 1);
-                        if (rdy && ns >= 1)
-                            rdy = tc::test_wait(smem_u32(s_free), (ns - 1) & 1);
-                        if (__shfl_sync(FULL, rdy, 0)) {
-                            tc::fence_after();
-                            issue_s_now(ns, ns == gend - 1);
-                            ns++;
-                            prog = true;
-                        }
-                    }
-                    if (prog) {
-                        t_last = global_timer_ns();
-                    } else {
-                        __nanosleep(16);
-                        if (__shfl_sync(FULL, global_timer_ns() - t_last > 2000000000ull, 0)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                }
-                if (!ok)
-                    break;
-                g0 += it.nkt;
-                if (lane == 0)
-                    mbar_arrive(&item_free[n & 1]);
-            }
-            if (!ok && lane == 0)
-                flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
-            // every MMA issued has completed before TMEM is released
-            if (tc::elect_one())
-                tc::commit(smem_u32(mma_done));
+        // Warp 9 issues the MMAs of Q tile A, warp 10 those of tile B, so the two
+        // tiles' issue and barrier waits run side by side.  Each warp walks the
+        // item's key tiles in order with blocking waits: for key tile j, S_t(j);
+        // then P.V_t(j - 1).  One elected lane issues the MMAs and commits.  A
+        // K, V or Q stage is released by one arrival from each warp: the warp's
+        // commit after its MMAs that read it, or, for a stage its tile does not
+        // read, a commit once the stage's tile has landed (so the arrival always
+        // counts towards that tile's phase: the stage is refilled only after both
+        // warps arrived for its previous tile).
+        const int t = warp - kTcMmaWarp;
+        bool ok = true;
+        const uint32_t qt = smem_u32(sQ) + (uint32_t)t * kQTile;
+        // a negative scale is applied by negating Q (bit 13 of the descriptor)
+        const uint32_t idS = tc::idesc_bf16(kTcRows, kTcKeys, false) | (p.neg_scale ? 1u << 13 : 0u);
+        const uint32_t idO = tc::idesc_f16(kTcRows, D, true);
+        const uint32_t dS = tmem + kTcSCol + 64u * (uint32_t)t, dO = tmem + 128u * (uint32_t)t;
+        const uint32_t pP0 = tmem + kTcPCol + 64u * (uint32_t)t;
+        uint64_t *my_s_full = s_full(t), *my_s_free = s_free(t), *my_o_free = o_free(t);
+        int g0 = 0;    // K/V tiles of the previous items
+        int gq = 0;    // S/P tiles of this Q tile over the previous items
+        int used = 0;  // items in which this Q tile had work (its epilogues)
+        for (int n = 0; ok; n++) {
+            if (!(ok = __all_sync(FULL, mbar_wait(&item_ready[n & 1], (n >> 1) & 1))))
+                break;
+            const PrefillItem it = items[n & 1];
+            if (it.b < 0)
+                break;
+            if (!(ok = __all_sync(FULL, mbar_wait(q_full, n & 1))))
+                break;
+            tc::fence_after();
+            const int nk = it.nkt[t];
+            const int nkt = max(it.nkt[0], it.nkt[1]);
+            if (nk == 0 && tc::elect_one())
+                tc::commit(smem_u32(q_empty));  // this tile reads no Q this item
             __syncwarp();
-            mbar_wait(mma_done, 0);
+            for (int j = 0; j <= nkt && ok; j++) {
+                if (j < nkt) {
+                    const int gkt = g0 + j, s = gkt % kTcKStages;
+                    if (!(ok = __all_sync(FULL, mbar_wait(&k_full[s], (gkt / kTcKStages) & 1))))
+                        break;
+                    if (j < nk) {
+                        // S_t(j) into the tile's S buffer once its softmax has loaded
+                        // S_t(j - 1) (at most one phase behind: the next completion
+                        // needs S_t(j), issued below)
+                        const int gs = gq + j;
+                        if (gs >= 1 && !(ok = __all_sync(FULL, mbar_wait(my_s_free, (gs - 1) & 1))))
+                            break;
+                        tc::fence_after();
+                        const uint32_t ka = smem_u32(sK + (size_t)s * kTile);
+                        if (tc::elect_one()) {
+#pragma unroll
+                            for (int kq = 0; kq < D / 16; kq++) {
+                                const uint32_t off = (uint32_t)(kq >> 2) * kQHalf + (uint32_t)(kq & 3) * 32;
+                                const uint32_t offk = (uint32_t)(kq >> 2) * kTileHalf + (uint32_t)(kq & 3) * 32;
+                                tc::mma_ss(dS, tc::smem_desc(qt + off, 16, 1024),
+                                           tc::smem_desc(ka + offk, 16, 1024), idS, kq > 0);
+                            }
+                            tc::commit(smem_u32(my_s_full));
+                            tc::commit(smem_u32(&k_empty[s]));
+                            if (j == nk - 1)
+                                tc::commit(smem_u32(q_empty));
+                        }
+                    } else if (tc::elect_one()) {
+                        tc::commit(smem_u32(&k_empty[s]));  // a K tile this Q tile does not read
+                    }
+                    __syncwarp();
+                }
+                if (j >= 1) {
+                    const int jj = j - 1, gvt = g0 + jj, s = gvt % kTcVStages;
+                    if (jj < nk) {
+                        // P.V_t(jj) once P_t(jj) is written and both softmax groups
+                        // converted their shares of V tile jj
+                        const int gp = gq + jj;
+                        if (!(ok = __all_sync(FULL, mbar_wait(pv_ready(t, gp & 1), (gp >> 1) & 1))))
+                            break;
+                        if (!(ok = __all_sync(FULL, mbar_wait(&v_conv[s], (gvt / kTcVStages) & 1))))
+                            break;
+                        // the item's first P.V overwrites O: the tile's previous
+                        // epilogue must have read it out
+                        if (jj == 0 && used >= 1 && !(ok = __all_sync(FULL, mbar_wait(my_o_free, (used - 1) & 1))))
+                            break;
+                        tc::fence_after();
+                        const uint32_t va = smem_u32(sV + (size_t)s * kTile);
+                        const uint32_t pP = pP0 + (uint32_t)(gp & 1) * 32u;
+                        if (tc::elect_one()) {
+#pragma unroll
+                            for (int kk = 0; kk < kTcKeys / 16; kk++) {
+                                const uint64_t dv = tc::smem_desc(va + kk * 16 * 128, kTileHalf, 1024);
+                                tc::mma_ts(dO, pP + 8 * kk, dv, idO, (jj > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            tc::commit(smem_u32(pv_done(t, gp & 1)));
+                            tc::commit(smem_u32(&v_empty[s]));
+                        }
+                    } else {
+                        // a V tile this Q tile does not read: arrive once it is
+                        // converted (so its tile has landed)
+                        if (!(ok = __all_sync(FULL, mbar_wait(&v_conv[s], (gvt / kTcVStages) & 1))))
+                            break;
+                        if (tc::elect_one())
+                            tc::commit(smem_u32(&v_empty[s]));
+                    }
+                    __syncwarp();
+                }
+            }
+            if (!ok)
+                break;
+            g0 += nkt;
+            gq += nk;
+            used += nk > 0 ? 1 : 0;
+            if (lane == 0)
+                mbar_arrive(&item_free[n & 1]);
         }
+        if (!ok && lane == 0)
+            flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
+        // every MMA issued has completed before TMEM is released
+        if (tc::elect_one())
+            tc::commit(smem_u32(mma_done));
+        __syncwarp();
+        mbar_wait(mma_done, 0);
         __syncwarp();
     } else {
         // ------------------------------------------------------------- softmax
-        const int r = threadIdx.x;            // row = TMEM lane
-        const uint32_t tl = (uint32_t)(32 * warp) << 16;
+        const int tq = warp >> 2;                       // Q tile of this group (A = 0, B = 1)
+        const int r = threadIdx.x & 127;                // row = TMEM lane
+        const uint32_t tl = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t tO = tmem + 128u * tq, tS = tmem + kTcSCol + 64u * tq;
+        const uint32_t tP0 = tmem + kTcPCol + 64u * tq;
         bool ok = true;
-        int g0 = 0;
+        int g0 = 0, gq = 0;
         for (int n = 0; ok; n++) {
             ok = __all_sync(FULL, mbar_wait(&item_ready[n & 1], (n >> 1) & 1));
             if (!ok)
@@ -597,253 +661,277 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const PrefillItem it = items[n & 1];
             if (it.b < 0)
                 break;
-            const int tok = it.tok0 + r / G, g = r % G;
+            const int nkt = it.nkt[tq], nk_other = it.nkt[1 - tq];
+            const int tok = it.tok0 + tq * TPC + r / G, g = r % G;
             const bool valid = tok < it.q_len;
             const int pos = (it.k_len - it.q_len) + tok;
             const int32_t *table = p.block_tables + (size_t)it.b * p.MBS;
-            const int nkt = it.nkt, k_len = it.k_len;
+            const int k_len = it.k_len;
             float m = -INFINITY, l = 0.f;
             uint32_t vmax = 0;  // f16 magnitudes of the converted V rows, max per half
-            // V_g in shared memory: bf16 -> f16 in place, rows past k_len or of
-            // unloaded boxes zeroed (their weight is 0, and 0 * NaN would be NaN);
-            // then P.V_g may be issued (P_g was written one tile earlier).  Done
-            // while the warps work on tile g + 1, so V_g has a tile more to land.
-            auto convert_v = [&](int gv, uint32_t vmask_bits, int kb) -> bool {
-                const int sv = gv % kTcVStages;
+            // V tile jv in shared memory: bf16 -> f16 in place, rows past k_len or
+            // of unloaded boxes zeroed (their weight is 0, and 0 * NaN would be
+            // NaN).  Every softmax warp takes part in every V tile, in order: it
+            // waits for the tile to land, converts its share and arrives once on
+            // the stage's v_conv (8 arrivals).  The share is half of the 16-byte
+            // chunks when both Q tiles read the V tile, all of them when only this
+            // group's tile does, none when only the other's does; so no group's
+            // parity wait on a V stage can fall two phases behind.  A group's share
+            // of V tile j is done right after it has loaded S of key tile j.
+            auto convert_v = [&](int jv, uint32_t vmask_bits, int mode) -> bool {
+                const int gv = g0 + jv, sv = gv % kTcVStages, kb = jv * kTcKeys;
                 if (!__all_sync(FULL, mbar_wait(&v_full[sv], (gv / kTcVStages) & 1)))
                     return false;
                 uint4 *vt = reinterpret_cast<uint4 *>(sV + (size_t)sv * kTile);
                 const bool vmask = vmask_bits != 0xFu || kb + kTcKeys > k_len;
-                // every load first, then the conversions, then every store: thread r
-                // owns 16-byte chunks r + 128 u (chunk i: half i / 512, key row
-                // (i / 8) % 64, one of the row's eight column groups)
+                // thread r owns 16-byte chunks r + 128 u (chunk i: half i / 512,
+                // key row (i / 8) % 64, one of the row's eight column groups)
                 constexpr int NCH = HALVES * kTcKeys * 8 / 128;
-                uint4 w[NCH];
+                constexpr int NH = NCH / 2;
+                auto run = [&](int u0, auto nu_c) {
+                    constexpr int NU = decltype(nu_c)::value;
+                    uint4 w[NU];
 #pragma unroll
-                for (int u = 0; u < NCH; u++)
-                    w[u] = vt[r + 128 * u];
+                    for (int u = 0; u < NU; u++)
+                        w[u] = vt[r + 128 * (u0 + u)];
 #pragma unroll
-                for (int u = 0; u < NCH; u++) {
-                    w[u].x = bf16x2_to_f16x2_sat(w[u].x);
-                    w[u].y = bf16x2_to_f16x2_sat(w[u].y);
-                    w[u].z = bf16x2_to_f16x2_sat(w[u].z);
-                    w[u].w = bf16x2_to_f16x2_sat(w[u].w);
-                }
-                if (vmask) {  // the same for the whole CTA: a tile with rows to clear
-#pragma unroll
-                    for (int u = 0; u < NCH; u++) {
-                        const int kr = ((r + 128 * u) / 8) % kTcKeys;
-                        if (kb + kr >= k_len || !((vmask_bits >> (kr / kBox)) & 1u))
-                            w[u] = make_uint4(0u, 0u, 0u, 0u);
+                    for (int u = 0; u < NU; u++) {
+                        w[u].x = bf16x2_to_f16x2_sat(w[u].x);
+                        w[u].y = bf16x2_to_f16x2_sat(w[u].y);
+                        w[u].z = bf16x2_to_f16x2_sat(w[u].z);
+                        w[u].w = bf16x2_to_f16x2_sat(w[u].w);
                     }
-                }
+                    if (vmask) {  // the same for the whole CTA: a tile with rows to clear
 #pragma unroll
-                for (int u = 0; u < NCH; u++)
-                    vmax = f16x2_absmax(vmax, f16x2_absmax(f16x2_absmax(w[u].x, w[u].y),
-                                                           f16x2_absmax(w[u].z, w[u].w)));
+                        for (int u = 0; u < NU; u++) {
+                            const int kr = ((r + 128 * (u0 + u)) / 8) % kTcKeys;
+                            if (kb + kr >= k_len || !((vmask_bits >> (kr / kBox)) & 1u))
+                                w[u] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
 #pragma unroll
-                for (int u = 0; u < NCH; u++)
-                    vt[r + 128 * u] = w[u];
+                    for (int u = 0; u < NU; u++)
+                        vmax = f16x2_absmax(vmax, f16x2_absmax(f16x2_absmax(w[u].x, w[u].y),
+                                                               f16x2_absmax(w[u].z, w[u].w)));
+#pragma unroll
+                    for (int u = 0; u < NU; u++)
+                        vt[r + 128 * (u0 + u)] = w[u];
+                };
+                if (mode == 1)
+                    run(tq * NH, std::integral_constant<int, NH>());
+                else if (mode == 2)
+                    run(0, std::integral_constant<int, NCH>());
                 fence_proxy_async_smem();
-                tc::fence_before();  // also orders this warp's tcgen05.st of P_g
+                tc::fence_before();  // also orders this warp's tcgen05.st of P
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(&pv_ready[gv & 1]);
+                    mbar_arrive(&v_conv[sv]);
                 return true;
             };
-            uint32_t prev_mask = 0;
-            int prev_kb = 0;
-            // boxes of a tile the producer loads (block ids in [0, NB)); read from
-            // the table here, not from the producer, whose K stage may already hold
-            // a later tile.  Lanes 0-3 read the entries of the next tile one tile
-            // ahead, so the load's latency is off the softmax's path.
-            auto table_entry = [&](int jt) -> int {
-                const int key0 = jt * kTcKeys + (lane & 3) * kBox;
-                return (lane < 4 && jt < nkt && key0 < k_len) ? __ldg(table + key0 / p.bs) : -1;
-            };
-            int blk_next = table_entry(0);
-            for (int j = 0; j < nkt; j++) {
-                const int gt = g0 + j;
-                const int blk = blk_next;
-                blk_next = table_entry(j + 1);
-                const uint32_t mask = __ballot_sync(FULL, blk >= 0 && blk < p.NB) & 0xFu;
-                ok = __all_sync(FULL, mbar_wait(s_full, gt & 1));
+            // this group's share of V tile jv (it reads V tiles 0 .. nkt - 1)
+            auto share = [&](int jv) { return jv >= nkt ? 0 : (jv < nk_other ? 1 : 2); };
+            if (nkt > 0) {
+                // boxes of a tile the producer loads (block ids in [0, NB)); read
+                // from the table here, not from the producer, whose K stage may
+                // already hold a later tile.  Lanes 0-3 read the entries of the
+                // next tile one tile ahead, so the load's latency is off the path.
+                auto table_entry = [&](int jt) -> int {
+                    const int key0 = jt * kTcKeys + (lane & 3) * kBox;
+                    return (lane < 4 && jt < nkt && key0 < k_len) ? __ldg(table + key0 / p.bs) : -1;
+                };
+                int blk_next = table_entry(0);
+                for (int j = 0; j < nkt; j++) {
+                    const int gt = gq + j;
+                    const int blk = blk_next;
+                    blk_next = table_entry(j + 1);
+                    const uint32_t mask = __ballot_sync(FULL, blk >= 0 && blk < p.NB) & 0xFu;
+                    ok = __all_sync(FULL, mbar_wait(s_full(tq), gt & 1));
+                    if (!ok)
+                        break;
+                    tc::fence_after();
+                    // raw scores of this row; the scale is applied inside the exp2
+                    // argument (p.scale_log2 >= 0: a negative scale negates Q in the MMA)
+                    float x[kTcKeys];
+                    {
+                        uint32_t ra[32], rb[32];
+                        tc::ld32(tS + tl, ra);
+                        tc::ld32(tS + tl + 32, rb);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i++) {
+                            x[i] = __uint_as_float(ra[i]);
+                            x[32 + i] = __uint_as_float(rb[i]);
+                        }
+                    }
+                    // S is in registers: the MMA warp may issue the next S into the buffer
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(s_free(tq));
+                    if (!(ok = convert_v(j, mask, share(j))))
+                        break;
+                    const int key_base = j * kTcKeys;
+                    // masked keys: past this row's position (the diagonal tiles) or
+                    // in an unloaded box.  Most tiles have none in the whole warp:
+                    // they take the paths without any per-key select.
+                    const bool masked = mask != 0xFu || key_base + kTcKeys - 1 > pos;
+                    const bool any_masked = __any_sync(FULL, masked);
+                    if (any_masked) {
+                        const int lim = pos - key_base;  // keys i > lim are in the future
+#pragma unroll
+                        for (int i = 0; i < kTcKeys; i++)
+                            x[i] = (i > lim || !((mask >> (i / kBox)) & 1u)) ? -INFINITY : x[i];
+                    }
+                    float mraw;
+                    {
+                        float t8[8];
+#pragma unroll
+                        for (int i = 0; i < 8; i++)
+                            t8[i] = x[i];
+#pragma unroll
+                        for (int i = 8; i < kTcKeys; i++)
+                            t8[i & 7] = fmaxf(t8[i & 7], x[i]);
+                        mraw = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
+                                     fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+                    }
+                    const float sl = p.scale_log2;
+                    const float mx = mraw == -INFINITY ? -INFINITY : mraw * sl;
+                    if (__any_sync(FULL, mx > m + kLazy)) {
+                        const float mn = fmaxf(m, mx);
+                        const float alpha = mn == -INFINITY ? 1.f : fast_exp2(m - mn);
+                        if (j > 0) {
+                            // O holds P_0..P_{j-1} V: rescale once the last P.V
+                            // completed (its V tile was converted above; pv_done of its
+                            // P buffer is at most one phase behind: the buffer's
+                            // previous P.V was awaited before P_{j-1} was written, and
+                            // its next one needs this group's next P)
+                            if (!(ok = __all_sync(FULL, mbar_wait(pv_done(tq, (gt - 1) & 1),
+                                                                  ((gt - 1) >> 1) & 1))))
+                                break;
+                            tc::fence_after();
+#pragma unroll 1
+                            for (int cc = 0; cc < D / 32; cc++) {
+                                uint32_t ro[32];
+                                tc::ld32(tO + tl + 32 * cc, ro);
+                                tc::wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 32; i++)
+                                    ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+                                tc::st32(tO + tl + 32 * cc, ro);
+                            }
+                            tc::wait_st();
+                        }
+                        l *= alpha;
+                        m = mn;
+                    }
+                    const float nmu = m == -INFINITY ? 0.f : -m;
+                    uint32_t pk[32];
+                    {
+                        // p = exp2(x sl - m), two keys per packed f32x2 FMA and add
+                        const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(nmu, nmu);
+                        float2 ls0 = make_float2(0.f, 0.f), ls1 = ls0;
+                        if (!any_masked) {
+#pragma unroll
+                            for (int i = 0; i < 32; i++) {
+                                const float2 a = ffma2(make_float2(x[2 * i], x[2 * i + 1]), sl2, nm2);
+                                const float2 e = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                                if (i & 1)
+                                    ls1 = fadd2(ls1, e);
+                                else
+                                    ls0 = fadd2(ls0, e);
+                                pk[i] = pack_f16x2(e.x, e.y);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; i++) {
+                                float2 a = ffma2(make_float2(x[2 * i], x[2 * i + 1]), sl2, nm2);
+                                // exact zeros for masked keys (also when the scale is 0,
+                                // where -inf * 0 would be NaN): exp2(-inf) = 0
+                                a.x = x[2 * i] == -INFINITY ? -INFINITY : a.x;
+                                a.y = x[2 * i + 1] == -INFINITY ? -INFINITY : a.y;
+                                const float2 e = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                                if (i & 1)
+                                    ls1 = fadd2(ls1, e);
+                                else
+                                    ls0 = fadd2(ls0, e);
+                                pk[i] = pack_f16x2(e.x, e.y);
+                            }
+                        }
+                        l += (ls0.x + ls0.y) + (ls1.x + ls1.y);
+                    }
+                    // P buffer gt & 1 was last read by P.V of tile gt - 2: wait for
+                    // it.  At most one phase behind: the P.V of tile gt - 4 was
+                    // awaited before P of tile gt - 2 was written, and the P.V of
+                    // tile gt needs the P written below.
+                    if (gt >= 2) {
+                        if (!(ok = __all_sync(FULL, mbar_wait(pv_done(tq, gt & 1), ((gt - 2) >> 1) & 1))))
+                            break;
+                        tc::fence_after();
+                    }
+                    tc::st32(tP0 + (uint32_t)(gt & 1) * 32u + tl, pk);
+                    tc::wait_st();
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(pv_ready(tq, gt & 1));
+                }
+            }
+            // V tiles of this item that only the other Q tile reads: no share to
+            // convert, but this group arrives on them in order too
+            for (int jv = nkt; ok && jv < max(it.nkt[0], it.nkt[1]); jv++)
+                ok = convert_v(jv, 0xFu, 0);
+            if (!ok)
+                break;
+            if (nkt > 0) {
+                // a converted V value was clamped to +-65504 (beyond f16's range):
+                // bf16 values at or below 65280 convert exactly, so only a clamp
+                // gives 0x7bff
+                if ((vmax & 0x7fffu) >= 0x7bffu || ((vmax >> 16) & 0x7fffu) >= 0x7bffu)
+                    flag_error(p.err_flag, kFlagVRange);
+                // the tile's last P.V done (its pv_done is at most one phase
+                // behind: the next P.V into that buffer needs this group's next P)
+                const int gl = gq + nkt - 1;
+                ok = __all_sync(FULL, mbar_wait(pv_done(tq, gl & 1), (gl >> 1) & 1));
                 if (!ok)
                     break;
                 tc::fence_after();
-                // raw scores of this row; the scale is applied inside the exp2
-                // argument (p.scale_log2 >= 0: a negative scale negates Q in the MMA)
-                float x[kTcKeys];
-                {
-                    uint32_t ra[32], rb[32];
-                    tc::ld32(tS + tl, ra);
-                    tc::ld32(tS + tl + 32, rb);
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                uint16_t *dst = p.out + ((size_t)(it.cq0 + tok) * p.Hq + it.kvh * G + g) * D;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; cc++) {
+                    uint32_t ro[32];
+                    tc::ld32(tO + tl + 32 * cc, ro);
                     tc::wait_ld();
+                    if (valid) {
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 32; i++) {
-                        x[i] = __uint_as_float(ra[i]);
-                        x[32 + i] = __uint_as_float(rb[i]);
+                        for (int i = 0; i < 16; i++)
+                            pk[i] = pack_bf16x2(__uint_as_float(ro[2 * i]) * inv,
+                                                __uint_as_float(ro[2 * i + 1]) * inv);
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * cc);
+#pragma unroll
+                        for (int i = 0; i < 4; i++)
+                            d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                     }
                 }
-                // S is in registers: the MMA warp may issue S_{g+1} into the buffer
+                // O read out: the tile's next first P.V may overwrite it
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(s_free);
-                if (j > 0 && !(ok = convert_v(gt - 1, prev_mask, prev_kb)))
-                    break;
-                const int key_base = j * kTcKeys;
-                // masked keys: past this row's position (the diagonal tiles) or in
-                // an unloaded box.  Most tiles have none in the whole warp: they
-                // take the paths without any per-key select.
-                const bool masked = mask != 0xFu || key_base + kTcKeys - 1 > pos;
-                const bool any_masked = __any_sync(FULL, masked);
-                if (any_masked) {
-                    const int lim = pos - key_base;  // keys i > lim are in the future
-#pragma unroll
-                    for (int i = 0; i < kTcKeys; i++)
-                        x[i] = (i > lim || !((mask >> (i / kBox)) & 1u)) ? -INFINITY : x[i];
-                }
-                float mraw;
-                {
-                    float t[8];
-#pragma unroll
-                    for (int i = 0; i < 8; i++)
-                        t[i] = x[i];
-#pragma unroll
-                    for (int i = 8; i < kTcKeys; i++)
-                        t[i & 7] = fmaxf(t[i & 7], x[i]);
-                    mraw = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])),
-                                 fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7])));
-                }
-                const float sl = p.scale_log2;
-                const float mx = mraw == -INFINITY ? -INFINITY : mraw * sl;
-                if (__any_sync(FULL, mx > m + kLazy)) {
-                    const float mn = fmaxf(m, mx);
-                    const float alpha = mn == -INFINITY ? 1.f : fast_exp2(m - mn);
-                    if (j > 0) {
-                        // O holds P_0..P_{j-1} V: rescale once the last P.V completed
-                        // (its pv_ready was arrived above; pv_done of its P buffer is at
-                        // most one phase behind: the buffer's previous P.V was awaited
-                        // before P_{g-1} was written, and its next one needs this
-                        // warp's next P)
-                        if (!(ok = __all_sync(FULL, mbar_wait(&pv_done[(gt - 1) & 1],
-                                                              ((gt - 1) >> 1) & 1))))
-                            break;
-                        tc::fence_after();
-#pragma unroll 1
-                        for (int cc = 0; cc < D / 32; cc++) {
-                            uint32_t ro[32];
-                            tc::ld32(tO + tl + 32 * cc, ro);
-                            tc::wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; i++)
-                                ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
-                            tc::st32(tO + tl + 32 * cc, ro);
-                        }
-                        tc::wait_st();
-                    }
-                    l *= alpha;
-                    m = mn;
-                }
-                const float nmu = m == -INFINITY ? 0.f : -m;
-                uint32_t pk[32];
-                {
-                    // p = exp2(x sl - m), two keys per packed f32x2 FMA and add
-                    const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(nmu, nmu);
-                    float2 ls0 = make_float2(0.f, 0.f), ls1 = ls0;
-                    if (!any_masked) {
-#pragma unroll
-                        for (int i = 0; i < 32; i++) {
-                            const float2 a = ffma2(make_float2(x[2 * i], x[2 * i + 1]), sl2, nm2);
-                            const float2 e = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-                            if (i & 1)
-                                ls1 = fadd2(ls1, e);
-                            else
-                                ls0 = fadd2(ls0, e);
-                            pk[i] = pack_f16x2(e.x, e.y);
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; i++) {
-                            float2 a = ffma2(make_float2(x[2 * i], x[2 * i + 1]), sl2, nm2);
-                            // exact zeros for masked keys (also when the scale is 0,
-                            // where -inf * 0 would be NaN): exp2(-inf) = 0
-                            a.x = x[2 * i] == -INFINITY ? -INFINITY : a.x;
-                            a.y = x[2 * i + 1] == -INFINITY ? -INFINITY : a.y;
-                            const float2 e = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-                            if (i & 1)
-                                ls1 = fadd2(ls1, e);
-                            else
-                                ls0 = fadd2(ls0, e);
-                            pk[i] = pack_f16x2(e.x, e.y);
-                        }
-                    }
-                    l += (ls0.x + ls0.y) + (ls1.x + ls1.y);
-                }
-                // P buffer gt & 1 was last read by P.V_{gt-2}: wait for it.  At most
-                // one phase behind: P.V_{gt-4} was awaited before P_{gt-2} was
-                // written, and P.V_gt needs the V conversion of the next step.
-                if (gt >= 2) {
-                    if (!(ok = __all_sync(FULL, mbar_wait(&pv_done[gt & 1], ((gt - 2) >> 1) & 1))))
-                        break;
-                    tc::fence_after();
-                }
-                tc::st32(tP0 + (uint32_t)(gt & 1) * (kTcKeys / 2) + tl, pk);
-                tc::wait_st();
-                prev_mask = mask;
-                prev_kb = key_base;
+                    mbar_arrive(o_free(tq));
             }
-            // the item's last V tile, after which its last P.V may run
-            if (ok)
-                ok = convert_v(g0 + nkt - 1, prev_mask, prev_kb);
-            // a converted V value was clamped to +-65504 (beyond f16's range): bf16
-            // values at or below 65280 convert exactly, so only a clamp gives 0x7bff
-            if (ok && ((vmax & 0x7fffu) >= 0x7bffu || ((vmax >> 16) & 0x7fffu) >= 0x7bffu))
-                flag_error(p.err_flag, kFlagVRange);
-            if (!ok)
-                break;
-            // the item's last P.V done (its pv_done is at most one phase behind:
-            // the next P.V in that buffer needs this warp's next P)
-            const int gl = g0 + nkt - 1;
-            ok = __all_sync(FULL, mbar_wait(&pv_done[gl & 1], (gl >> 1) & 1));
-            if (!ok)
-                break;
-            tc::fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint16_t *dst = p.out + ((size_t)(it.cq0 + tok) * p.Hq + it.kvh * G + g) * D;
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; cc++) {
-                uint32_t ro[32];
-                tc::ld32(tO + tl + 32 * cc, ro);
-                tc::wait_ld();
-                if (valid) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        pk[i] = pack_bf16x2(__uint_as_float(ro[2 * i]) * inv,
-                                            __uint_as_float(ro[2 * i + 1]) * inv);
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * cc);
-#pragma unroll
-                    for (int i = 0; i < 4; i++)
-                        d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
-            }
-            // O read out: the next item's first P.V may overwrite it
-            tc::fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(o_free);
+            if (lane == 0)
                 mbar_arrive(&item_free[n & 1]);
-            }
-            g0 += nkt;
+            g0 += max(it.nkt[0], it.nkt[1]);
+            gq += nkt;
         }
         if (!ok && lane == 0)
             flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kTcMmaWarp) {
         tc::fence_after();
         tc::dealloc(tmem, kTcCols);
     }

@@ -22,6 +22,11 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// SM cycle counter: cheap to read (unlike %globaltimer), for the polling
+// loops' give-up limit.  kPollLimitCycles is about two seconds at 2 GHz.
+__device__ __forceinline__ uint64_t sm_clock() { return (uint64_t)clock64(); }
+constexpr uint64_t kPollLimitCycles = 4000000000ull;
+
 // ---- programmatic dependent launch -------------------------------------
 // Block until the grids this one depends on have completed and their memory
 // is visible (no-op without a programmatic dependency).
