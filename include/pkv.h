@@ -196,6 +196,18 @@ pkv_status pkv_paged_attn_decode(const void *q, const void *k_cache, const void 
  * PKV_FLAG_BAD_BLOCK and its 16-token boxes are left out of the softmax.
  * Host-side errors return a status before any launch; B, Tq or
  * max_seqlen_q == 0 is a no-op.
+ *
+ * Precision: q . K^T runs on the tensor cores in bf16 with fp32
+ * accumulation; P . V runs in f16 with fp32 accumulation: P (at most 2^8
+ * after the online max) is rounded to f16, and V to f16, which holds every
+ * bf16 value of magnitude in [2^-17, 65504] exactly (smaller magnitudes
+ * round to f16 subnormals, absolute error <= 2^-25).  V values beyond
+ * +-65504 (and infinities) are clamped to +-65504 and set PKV_FLAG_V_RANGE;
+ * NaN stays NaN.  Output rounded to bf16.
+ *
+ * The kernel runs one CTA per SM that holds all of the SM's tensor memory
+ * (512 columns); a concurrent kernel that allocates tensor memory on the
+ * same SMs waits for it.
  */
 pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *block_tables, int MBS, const int32_t *cu_seqlens_q,
