@@ -217,6 +217,28 @@ pkv_status make_cache_map(CUtensorMap *map, const void *cache, long long tokens,
     return PKV_OK;
 }
 
+// The same cache for the prefill kernel's whole-tile copies, where a block
+// holds whole 64-token tiles (bs % 64 == 0): 4-D (64 columns, tokens, Hkv,
+// D/64 halves), box 64 x 64 x 1 x D/64, landing as the tile's halves one after
+// the other, each 64 rows of 128 B with the 128-byte swizzle (the layout the
+// score and P.V MMAs read).
+pkv_status make_cache_tile_map(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc)
+        return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[4] = {64, (cuuint64_t)tokens, (cuuint64_t)Hkv, (cuuint64_t)(D / 64)};
+    cuuint64_t strides[3] = {(cuuint64_t)Hkv * D * 2, (cuuint64_t)D * 2, 128};
+    cuuint32_t box[4] = {64, (cuuint32_t)pkv::kPrefillKeys, 1, (cuuint32_t)(D / 64)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (tile) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
 // Prefill queries q [Tq, Hq, D] bf16 as 4-D (64, D/64, Hq, Tq) like the cache;
 // box 64 x 1 x G x 128/G: one 128-row (token, head) tile half per copy.
 pkv_status make_q_map(CUtensorMap *map, const void *q, long long Tq, int Hq, int D, int G)
@@ -259,11 +281,14 @@ pkv_status make_cache_map8(CUtensorMap *map, const void *cache, long long tokens
 
 // Tensor maps of recently used caches, per host thread (a map is plain data:
 // the same cache pointer and shape always encode the same map).
+// Map kinds: 16-token boxes of a bf16 cache, of an FP8 cache, or whole
+// 64-token prefill tiles of a bf16 cache.
+enum MapKind { kMapBox = 0, kMapBox8 = 1, kMapTile = 2 };
 struct MapEntry {
     const void *ptr = nullptr;
     long long tokens = 0;
     int Hkv = 0, D = 0;
-    bool f8 = false;
+    int kind = kMapBox;
     CUtensorMap map;
 };
 constexpr int kMapCache = 8;
@@ -271,15 +296,16 @@ thread_local MapEntry t_maps[kMapCache];
 thread_local int t_map_next = 0;
 
 pkv_status cached_cache_map(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D,
-                            bool f8 = false)
+                            int kind = kMapBox)
 {
     for (const auto &e : t_maps)
-        if (e.ptr == cache && e.tokens == tokens && e.Hkv == Hkv && e.D == D && e.f8 == f8) {
+        if (e.ptr == cache && e.tokens == tokens && e.Hkv == Hkv && e.D == D && e.kind == kind) {
             *map = e.map;
             return PKV_OK;
         }
-    const pkv_status ps = f8 ? make_cache_map8(map, cache, tokens, Hkv, D)
-                             : make_cache_map(map, cache, tokens, Hkv, D);
+    const pkv_status ps = kind == kMapBox8   ? make_cache_map8(map, cache, tokens, Hkv, D)
+                          : kind == kMapTile ? make_cache_tile_map(map, cache, tokens, Hkv, D)
+                                             : make_cache_map(map, cache, tokens, Hkv, D);
     if (ps != PKV_OK)
         return ps;
     MapEntry &e = t_maps[t_map_next];
@@ -288,7 +314,7 @@ pkv_status cached_cache_map(CUtensorMap *map, const void *cache, long long token
     e.tokens = tokens;
     e.Hkv = Hkv;
     e.D = D;
-    e.f8 = f8;
+    e.kind = kind;
     e.map = *map;
     return PKV_OK;
 }
@@ -448,9 +474,9 @@ static pkv_status decode_impl(const void *q, const void *k_cache, const void *v_
 
     CUtensorMap tmk, tmv;
     const long long tokens = (long long)NB * bs;
-    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D, f8)) != PKV_OK)
+    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D, f8 ? kMapBox8 : kMapBox)) != PKV_OK)
         return ps;
-    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D, f8)) != PKV_OK)
+    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D, f8 ? kMapBox8 : kMapBox)) != PKV_OK)
         return ps;
 
     pkv::DecodeParams p;
@@ -621,9 +647,13 @@ pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_c
     }
     CUtensorMap tmq, tmk, tmv;
     const long long tokens = (long long)NB * bs;
-    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D)) != PKV_OK)
+    // blocks of whole 64-token tiles: one copy per K or V tile, else one per
+    // 16-token box and 64-column half
+    const bool tile_copies = bs % pkv::kPrefillKeys == 0;
+    const int kind = tile_copies ? kMapTile : kMapBox;
+    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D, kind)) != PKV_OK)
         return ps;
-    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D)) != PKV_OK)
+    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D, kind)) != PKV_OK)
         return ps;
     if ((ps = make_q_map(&tmq, q, Tq, Hq, D, G)) != PKV_OK)
         return ps;
@@ -646,6 +676,7 @@ pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_c
     p.n_items = (int)(pairs * Hkv * B);
     p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
     p.neg_scale = scale < 0.f;
+    p.tile_copies = tile_copies ? 1 : 0;
     // Persistent grid: one CTA per SM (each holds all of the SM's TMEM
     // columns, and asks for more than half of its shared memory so that no
     // second CTA lands beside it), each walking its share of the work items.

@@ -23,6 +23,7 @@ struct PrefillParams {
     int n_items;                  // work items: X tile pairs x Hkv heads x B sequences
     float scale_log2;             // |scale| * log2(e)
     int neg_scale;                // scale < 0: the score MMA negates Q
+    int tile_copies;              // bs % 64 == 0: K/V maps copy whole 64-token tiles
 };
 
 cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmq, const CUtensorMap *tmk,
@@ -31,6 +32,7 @@ cudaError_t launch_prefill(int D, int G, const CUtensorMap *tmq, const CUtensorM
 const void *prefill_kernel(int D, int G);
 size_t prefill_smem_bytes(int D);
 constexpr int kPrefillRows = 128;  // (token, head) rows per query tile (two tiles per work item)
+constexpr int kPrefillKeys = 64;   // keys per K/V tile
 constexpr int kPrefillThreads = 11 * 32;
 
 } // namespace pkv

@@ -15,25 +15,26 @@
 // each item through a two-slot buffer, and every ring, S, P and P.V phase
 // runs on over a CTA's items.  Warps:
 //   0..3  softmax of tile A, 4..7 softmax of tile B: thread t of a group owns
-//         row t (TMEM lane t).  Per 64-key tile: load S from TMEM and hand the
-//         S buffer back at once, exponentiate, write P (f16) into one of the
-//         tile's two P buffers, and convert the previous V tile in shared
-//         memory from bf16 to f16 (rows past k_len or of unloaded boxes
-//         zeroed), each group one half of it when both tiles read it
+//         row t (TMEM lane t).  Per 64-key tile: load S from TMEM, convert
+//         the V tile in shared memory from bf16 to f16 (rows past k_len or of
+//         unloaded boxes zeroed; each group one half of it when both tiles
+//         read it), exponentiate, and write P (f16) over the row's S
 //   8     producer: finds the next item, TMA of its Q tiles, then 64-key K and
-//         V tiles (four 16-token boxes each, resolved through the block
-//         table) into separate 4-stage rings
-//   9     MMA: allocates all 512 TMEM columns and issues, as the operands
-//         become ready (P.V first, so V stages return early):
+//         V tiles into separate 4-stage rings: one copy per tile where the
+//         block size is a multiple of 64, else four 16-token boxes per tile
+//         and half, each resolved through the block table
+//   9, 10 MMA of tiles A and B (warp 9 allocates all 512 TMEM columns); per
+//         key tile j, in order: S_t(j), then P.V_t(j - 1):
 //           S_t = Q_t K_j^T   (SS, bf16, K-major 128-byte-swizzled, M=128 N=64)
 //           O_t += P_t V_j    (TS, f16: P from TMEM, V MN-major, N=D)
-// TMEM columns: O_A [0, D), O_B [128, 128 + D), S_A 256, S_B 320 (64 f32
-// columns each), P buffers at 384 (A) and 448 (B), two of 32 columns each
-// (64 f16 keys).  S_t(j+1) is issued once the group has loaded S_t(j), and
-// runs while it works on S_t(j); the group writes P_t(j) only after the P.V
-// that read the same P buffer (P.V_t(j-2)) has completed (MMAs are not
-// ordered against each other's TMEM accesses); an item's first P.V of a tile
-// waits until that tile's previous epilogue has read O out.
+// TMEM columns: O_A [0, D), O_B [128, 128 + D), two S buffers per tile (64
+// f32 columns each) at 256 + 128 t + 64 b; P_t(j) (64 f16 keys, 32 columns)
+// is written over S_t(j) once the row's S is in registers.  S_t(j + 1) goes
+// into the other buffer and runs while the group works on S_t(j); S_t(j + 2)
+// is issued only after P.V_t(j), which reads P_t(j) from its buffer, has
+// completed (MMAs are not ordered against each other's TMEM accesses); an
+// item's first P.V of a tile waits until that tile's previous epilogue has
+// read O out.
 // P.V in f16: P = exp2(...) <= 2^8 is rounded to f16 (11 significant bits),
 // and V is converted to f16, exact for every bf16 value of magnitude in
 // [2^-14, 65504] (and for any bf16 value >= 2^-17); smaller magnitudes round
@@ -65,8 +66,8 @@ constexpr int kTcThreads = kPrefillThreads;  // 8 softmax warps, producer, 2 MMA
 constexpr int kTcProducerWarp = 8;
 constexpr int kTcMmaWarp = 9;           // warps 9 and 10 issue the MMAs of tiles A and B
 constexpr uint32_t kTcCols = 512;       // all of the SM's TMEM columns
-constexpr uint32_t kTcSCol = 256;       // S_t at 256 + 64 t (64 f32 columns)
-constexpr uint32_t kTcPCol = 384;       // P_t buffers at 384 + 64 t + 32 b (64 f16 keys)
+constexpr uint32_t kTcSCol = 256;       // S_t buffers at 256 + 128 t + 64 b (64 f32 columns);
+                                        // P_t(j) (64 f16 keys, 32 columns) over S_t(j)
 constexpr int kFlagVRange = 0x10;       // PKV_FLAG_V_RANGE (pkv.h)
 // More than half an SM's shared memory, so that one CTA (which holds every
 // TMEM column) runs per SM.
@@ -77,7 +78,7 @@ struct TcSmem {
 };
 
 // Barriers: q_full, q_empty, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
-// v_conv[VS], then per Q tile: s_full, s_free, pv_ready[2], pv_done[2], o_free;
+// v_conv[VS], then per Q tile: s_full[2], pv_ready[2], pv_done[2], o_free;
 // then item_ready[2], item_free[2], mma_done.
 constexpr int kTcTileBars = 7;
 constexpr int kTcBars = 2 + 2 * kTcKStages + 3 * kTcVStages + 2 * kTcTileBars + 2 + 2 + 1;
@@ -275,11 +276,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *item_ready = tbar + 2 * kTcTileBars; // [2] item parameters published
     uint64_t *item_free = item_ready + 2;          // [2] item parameters no longer needed
     uint64_t *mma_done = item_free + 2;            // every MMA of the CTA completed
-    // per Q tile t: s_full (S_t written), s_free (S_t loaded by the tile's four
-    // softmax warps), pv_ready[2] (P_t written, by P buffer), pv_done[2] (P.V_t
-    // completed, by P buffer), o_free (the tile's O read out by its epilogue)
-    auto s_full = [&](int t) { return tbar + kTcTileBars * t; };
-    auto s_free = [&](int t) { return tbar + kTcTileBars * t + 1; };
+    // per Q tile t and S buffer b: s_full[b] (S_t written), pv_ready[b] (P_t
+    // written over it), pv_done[b] (the P.V_t that read that P completed); and
+    // o_free (the tile's O read out by its epilogue)
+    auto s_full = [&](int t, int b) { return tbar + kTcTileBars * t + b; };
     auto pv_ready = [&](int t, int b) { return tbar + kTcTileBars * t + 2 + b; };
     auto pv_done = [&](int t, int b) { return tbar + kTcTileBars * t + 4 + b; };
     auto o_free = [&](int t) { return tbar + kTcTileBars * t + 6; };
@@ -305,9 +305,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&v_conv[s], 8);  // one share per softmax warp
         }
         for (int t = 0; t < 2; t++) {
-            mbar_init(s_full(t), 1);
-            mbar_init(s_free(t), 4);
             for (int b = 0; b < 2; b++) {
+                mbar_init(s_full(t, b), 1);
                 mbar_init(pv_ready(t, b), 4);
                 mbar_init(pv_done(t, b), 1);
             }
@@ -464,17 +463,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 } else {
                     row = get_row(j);
                 }
-                const bool loaded = row >= 0;
-                const uint32_t mask = __ballot_sync(FULL, loaded);
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&fb[s], (uint32_t)__popc(mask) * kBoxBytes);
-                __syncwarp();
-                if (loaded) {
-                    uint8_t *dst = (is_k ? sK : sV) + (size_t)s * kTile + lane * (kBox * 128);
-                    const CUtensorMap *map = is_k ? &tmk : &tmv;
+                const CUtensorMap *map = is_k ? &tmk : &tmv;
+                uint8_t *dst = (is_k ? sK : sV) + (size_t)s * kTile;
+                if (p.tile_copies) {
+                    // the tile's 64 tokens lie in one block: one copy of the
+                    // whole tile, both halves (rows past k_len included: the
+                    // softmax masks their scores and zeroes their V rows)
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&fb[s], row >= 0 ? kTile : 0u);
+                        if (row >= 0)
+                            tma_load_4d(dst, map, 0, row, it.kvh, 0, &fb[s]);
+                    }
+                } else {
+                    const bool loaded = row >= 0;
+                    const uint32_t mask = __ballot_sync(FULL, loaded);
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&fb[s], (uint32_t)__popc(mask) * kBoxBytes);
+                    __syncwarp();
+                    if (loaded) {
 #pragma unroll
-                    for (int h = 0; h < HALVES; h++)
-                        tma_load_4d(dst + h * kTileHalf, map, 0, h, it.kvh, row, &fb[s]);
+                        for (int h = 0; h < HALVES; h++)
+                            tma_load_4d(dst + lane * (kBox * 128) + h * kTileHalf, map, 0, h, it.kvh, row,
+                                        &fb[s]);
+                    }
                 }
             };
             int jk = 0, jv = 0;
@@ -528,7 +539,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // Warp 9 issues the MMAs of Q tile A, warp 10 those of tile B, so the two
         // tiles' issue and barrier waits run side by side.  Each warp walks the
         // item's key tiles in order with blocking waits: for key tile j, S_t(j);
-        // then P.V_t(j - 1).  One elected lane issues the MMAs and commits.  A
+        // then P.V_t(j - 1).  Lane 0 alone waits, issues the MMAs and commits.  A
         // K, V or Q stage is released by one arrival from each warp: the warp's
         // commit after its MMAs that read it, or, for a stage its tile does not
         // read, a commit once the stage's tile has landed (so the arrival always
@@ -540,107 +551,107 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // a negative scale is applied by negating Q (bit 13 of the descriptor)
         const uint32_t idS = tc::idesc_bf16(kTcRows, kTcKeys, false) | (p.neg_scale ? 1u << 13 : 0u);
         const uint32_t idO = tc::idesc_f16(kTcRows, D, true);
-        const uint32_t dS = tmem + kTcSCol + 64u * (uint32_t)t, dO = tmem + 128u * (uint32_t)t;
-        const uint32_t pP0 = tmem + kTcPCol + 64u * (uint32_t)t;
-        uint64_t *my_s_full = s_full(t), *my_s_free = s_free(t), *my_o_free = o_free(t);
+        const uint32_t dS0 = tmem + kTcSCol + 128u * (uint32_t)t, dO = tmem + 128u * (uint32_t)t;
+        uint64_t *my_o_free = o_free(t);
         int g0 = 0;    // K/V tiles of the previous items
         int gq = 0;    // S/P tiles of this Q tile over the previous items
         int used = 0;  // items in which this Q tile had work (its epilogues)
-        for (int n = 0; ok; n++) {
-            if (!(ok = __all_sync(FULL, mbar_wait(&item_ready[n & 1], (n >> 1) & 1))))
-                break;
-            const PrefillItem it = items[n & 1];
-            if (it.b < 0)
-                break;
-            if (!(ok = __all_sync(FULL, mbar_wait(q_full, n & 1))))
-                break;
-            tc::fence_after();
-            const int nk = it.nkt[t];
-            const int nkt = max(it.nkt[0], it.nkt[1]);
-            if (nk == 0 && tc::elect_one())
-                tc::commit(smem_u32(q_empty));  // this tile reads no Q this item
-            __syncwarp();
-            for (int j = 0; j <= nkt && ok; j++) {
-                if (j < nkt) {
-                    const int gkt = g0 + j, s = gkt % kTcKStages;
-                    if (!(ok = __all_sync(FULL, mbar_wait(&k_full[s], (gkt / kTcKStages) & 1))))
-                        break;
-                    if (j < nk) {
-                        // S_t(j) into the tile's S buffer once its softmax has loaded
-                        // S_t(j - 1) (at most one phase behind: the next completion
-                        // needs S_t(j), issued below)
-                        const int gs = gq + j;
-                        if (gs >= 1 && !(ok = __all_sync(FULL, mbar_wait(my_s_free, (gs - 1) & 1))))
+        // lane 0 alone waits, issues the MMAs and commits
+        if (lane == 0) {
+            for (int n = 0; ok; n++) {
+                if (!(ok = mbar_wait(&item_ready[n & 1], (n >> 1) & 1)))
+                    break;
+                const PrefillItem it = items[n & 1];
+                if (it.b < 0)
+                    break;
+                if (!(ok = mbar_wait(q_full, n & 1)))
+                    break;
+                tc::fence_after();
+                const int nk = it.nkt[t];
+                const int nkt = max(it.nkt[0], it.nkt[1]);
+                if (nk == 0)
+                    tc::commit(smem_u32(q_empty));  // this tile reads no Q this item
+                for (int j = 0; j <= nkt && ok; j++) {
+                    if (j < nkt) {
+                        const int gkt = g0 + j, s = gkt % kTcKStages;
+                        if (!(ok = mbar_wait(&k_full[s], (gkt / kTcKStages) & 1)))
                             break;
-                        tc::fence_after();
-                        const uint32_t ka = smem_u32(sK + (size_t)s * kTile);
-                        if (tc::elect_one()) {
+                        if (j < nk) {
+                            // S_t(j) into S buffer gs & 1 once the P.V that read P_t(j - 2)
+                            // from it completed (at most one phase behind: the next
+                            // completion needs S_t(j), issued below; the one before was
+                            // awaited before S_t(j - 2))
+                            const int gs = gq + j;
+                            if (gs >= 2 && !(ok = mbar_wait(pv_done(t, gs & 1), ((gs - 2) >> 1) & 1)))
+                                break;
+                            tc::fence_after();
+                            const uint32_t ka = smem_u32(sK + (size_t)s * kTile);
+                            const uint32_t dS = dS0 + 64u * (uint32_t)(gs & 1);
+                            {
 #pragma unroll
-                            for (int kq = 0; kq < D / 16; kq++) {
-                                const uint32_t off = (uint32_t)(kq >> 2) * kQHalf + (uint32_t)(kq & 3) * 32;
-                                const uint32_t offk = (uint32_t)(kq >> 2) * kTileHalf + (uint32_t)(kq & 3) * 32;
-                                tc::mma_ss(dS, tc::smem_desc(qt + off, 16, 1024),
-                                           tc::smem_desc(ka + offk, 16, 1024), idS, kq > 0);
+                                for (int kq = 0; kq < D / 16; kq++) {
+                                    const uint32_t off = (uint32_t)(kq >> 2) * kQHalf + (uint32_t)(kq & 3) * 32;
+                                    const uint32_t offk = (uint32_t)(kq >> 2) * kTileHalf + (uint32_t)(kq & 3) * 32;
+                                    tc::mma_ss(dS, tc::smem_desc(qt + off, 16, 1024),
+                                               tc::smem_desc(ka + offk, 16, 1024), idS, kq > 0);
+                                }
+                                tc::commit(smem_u32(s_full(t, gs & 1)));
+                                tc::commit(smem_u32(&k_empty[s]));
+                                if (j == nk - 1)
+                                    tc::commit(smem_u32(q_empty));
                             }
-                            tc::commit(smem_u32(my_s_full));
-                            tc::commit(smem_u32(&k_empty[s]));
-                            if (j == nk - 1)
-                                tc::commit(smem_u32(q_empty));
+                        } else {
+                            tc::commit(smem_u32(&k_empty[s]));  // a K tile this Q tile does not read
                         }
-                    } else if (tc::elect_one()) {
-                        tc::commit(smem_u32(&k_empty[s]));  // a K tile this Q tile does not read
-                    }
-                    __syncwarp();
-                }
-                if (j >= 1) {
-                    const int jj = j - 1, gvt = g0 + jj, s = gvt % kTcVStages;
-                    if (jj < nk) {
-                        // P.V_t(jj) once P_t(jj) is written and both softmax groups
-                        // converted their shares of V tile jj
-                        const int gp = gq + jj;
-                        if (!(ok = __all_sync(FULL, mbar_wait(pv_ready(t, gp & 1), (gp >> 1) & 1))))
-                            break;
-                        if (!(ok = __all_sync(FULL, mbar_wait(&v_conv[s], (gvt / kTcVStages) & 1))))
-                            break;
-                        // the item's first P.V overwrites O: the tile's previous
-                        // epilogue must have read it out
-                        if (jj == 0 && used >= 1 && !(ok = __all_sync(FULL, mbar_wait(my_o_free, (used - 1) & 1))))
-                            break;
-                        tc::fence_after();
-                        const uint32_t va = smem_u32(sV + (size_t)s * kTile);
-                        const uint32_t pP = pP0 + (uint32_t)(gp & 1) * 32u;
-                        if (tc::elect_one()) {
-#pragma unroll
-                            for (int kk = 0; kk < kTcKeys / 16; kk++) {
-                                const uint64_t dv = tc::smem_desc(va + kk * 16 * 128, kTileHalf, 1024);
-                                tc::mma_ts(dO, pP + 8 * kk, dv, idO, (jj > 0 || kk > 0) ? 1u : 0u);
                             }
-                            tc::commit(smem_u32(pv_done(t, gp & 1)));
+                    if (j >= 1) {
+                        const int jj = j - 1, gvt = g0 + jj, s = gvt % kTcVStages;
+                        if (jj < nk) {
+                            // P.V_t(jj) once P_t(jj) is written and both softmax groups
+                            // converted their shares of V tile jj
+                            const int gp = gq + jj;
+                            if (!(ok = mbar_wait(pv_ready(t, gp & 1), (gp >> 1) & 1)))
+                                break;
+                            if (!(ok = mbar_wait(&v_conv[s], (gvt / kTcVStages) & 1)))
+                                break;
+                            // the item's first P.V overwrites O: the tile's previous
+                            // epilogue must have read it out
+                            if (jj == 0 && used >= 1 && !(ok = mbar_wait(my_o_free, (used - 1) & 1)))
+                                break;
+                            tc::fence_after();
+                            const uint32_t va = smem_u32(sV + (size_t)s * kTile);
+                            const uint32_t pP = dS0 + 64u * (uint32_t)(gp & 1);  // P_t(jj) over S_t(jj)
+                            {
+#pragma unroll
+                                for (int kk = 0; kk < kTcKeys / 16; kk++) {
+                                    const uint64_t dv = tc::smem_desc(va + kk * 16 * 128, kTileHalf, 1024);
+                                    tc::mma_ts(dO, pP + 8 * kk, dv, idO, (jj > 0 || kk > 0) ? 1u : 0u);
+                                }
+                                tc::commit(smem_u32(pv_done(t, gp & 1)));
+                                tc::commit(smem_u32(&v_empty[s]));
+                            }
+                        } else {
+                            // a V tile this Q tile does not read: arrive once it is
+                            // converted (so its tile has landed)
+                            if (!(ok = mbar_wait(&v_conv[s], (gvt / kTcVStages) & 1)))
+                                break;
                             tc::commit(smem_u32(&v_empty[s]));
                         }
-                    } else {
-                        // a V tile this Q tile does not read: arrive once it is
-                        // converted (so its tile has landed)
-                        if (!(ok = __all_sync(FULL, mbar_wait(&v_conv[s], (gvt / kTcVStages) & 1))))
-                            break;
-                        if (tc::elect_one())
-                            tc::commit(smem_u32(&v_empty[s]));
-                    }
-                    __syncwarp();
+                            }
                 }
-            }
-            if (!ok)
-                break;
-            g0 += nkt;
-            gq += nk;
-            used += nk > 0 ? 1 : 0;
-            if (lane == 0)
+                if (!ok)
+                    break;
+                g0 += nkt;
+                gq += nk;
+                used += nk > 0 ? 1 : 0;
                 mbar_arrive(&item_free[n & 1]);
+            }
         }
+        __syncwarp();
         if (!ok && lane == 0)
             flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
         // every MMA issued has completed before TMEM is released
-        if (tc::elect_one())
+        if (lane == 0)
             tc::commit(smem_u32(mma_done));
         __syncwarp();
         mbar_wait(mma_done, 0);
@@ -650,8 +661,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int tq = warp >> 2;                       // Q tile of this group (A = 0, B = 1)
         const int r = threadIdx.x & 127;                // row = TMEM lane
         const uint32_t tl = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tO = tmem + 128u * tq, tS = tmem + kTcSCol + 64u * tq;
-        const uint32_t tP0 = tmem + kTcPCol + 64u * tq;
+        const uint32_t tO = tmem + 128u * tq, tS0 = tmem + kTcSCol + 128u * tq;
         bool ok = true;
         int g0 = 0, gq = 0;
         for (int n = 0; ok; n++) {
@@ -745,10 +755,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int blk = blk_next;
                     blk_next = table_entry(j + 1);
                     const uint32_t mask = __ballot_sync(FULL, blk >= 0 && blk < p.NB) & 0xFu;
-                    ok = __all_sync(FULL, mbar_wait(s_full(tq), gt & 1));
+                    ok = __all_sync(FULL, mbar_wait(s_full(tq, gt & 1), (gt >> 1) & 1));
                     if (!ok)
                         break;
                     tc::fence_after();
+                    const uint32_t tS = tS0 + 64u * (uint32_t)(gt & 1);
                     // raw scores of this row; the scale is applied inside the exp2
                     // argument (p.scale_log2 >= 0: a negative scale negates Q in the MMA)
                     float x[kTcKeys];
@@ -763,11 +774,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             x[32 + i] = __uint_as_float(rb[i]);
                         }
                     }
-                    // S is in registers: the MMA warp may issue the next S into the buffer
-                    tc::fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(s_free(tq));
                     if (!(ok = convert_v(j, mask, share(j))))
                         break;
                     const int key_base = j * kTcKeys;
@@ -801,10 +807,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const float alpha = mn == -INFINITY ? 1.f : fast_exp2(m - mn);
                         if (j > 0) {
                             // O holds P_0..P_{j-1} V: rescale once the last P.V
-                            // completed (its V tile was converted above; pv_done of its
-                            // P buffer is at most one phase behind: the buffer's
-                            // previous P.V was awaited before P_{j-1} was written, and
-                            // its next one needs this group's next P)
+                            // completed (pv_done of its S buffer is at most one phase
+                            // behind: the buffer's previous P.V completed before
+                            // S_{j-1} was issued into it, and its next one needs this
+                            // group's next P)
                             if (!(ok = __all_sync(FULL, mbar_wait(pv_done(tq, (gt - 1) & 1),
                                                                   ((gt - 1) >> 1) & 1))))
                                 break;
@@ -859,16 +865,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         l += (ls0.x + ls0.y) + (ls1.x + ls1.y);
                     }
-                    // P buffer gt & 1 was last read by P.V of tile gt - 2: wait for
-                    // it.  At most one phase behind: the P.V of tile gt - 4 was
-                    // awaited before P of tile gt - 2 was written, and the P.V of
-                    // tile gt needs the P written below.
-                    if (gt >= 2) {
-                        if (!(ok = __all_sync(FULL, mbar_wait(pv_done(tq, gt & 1), ((gt - 2) >> 1) & 1))))
-                            break;
-                        tc::fence_after();
-                    }
-                    tc::st32(tP0 + (uint32_t)(gt & 1) * 32u + tl, pk);
+                    // P over this row's S (all of it is in registers; the next S
+                    // into the buffer waits for the P.V that reads this P)
+                    tc::st32(tS + tl, pk);
                     tc::wait_st();
                     tc::fence_before();
                     __syncwarp();
