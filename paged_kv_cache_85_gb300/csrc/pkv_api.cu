@@ -680,7 +680,7 @@ pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_c
     // Persistent grid: one CTA per SM (each holds all of the SM's TMEM
     // columns, and asks for more than half of its shared memory so that no
     // second CTA lands beside it), each walking its share of the work items.
-    static_assert(pkv::kPrefillThreads * 186 <= 65536, "prefill registers per thread");
+    static_assert(pkv::kPrefillThreads * 168 <= 65536, "prefill registers per thread");
     long long grid = (long long)st->sms;
     if (grid > p.n_items)
         grid = p.n_items;

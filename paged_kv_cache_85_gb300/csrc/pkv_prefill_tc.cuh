@@ -17,8 +17,9 @@
 //   0..3  softmax of tile A, 4..7 softmax of tile B: thread t of a group owns
 //         row t (TMEM lane t).  Per 64-key tile: load S from TMEM, convert
 //         the V tile in shared memory from bf16 to f16 (rows past k_len or of
-//         unloaded boxes zeroed; each group one half of it when both tiles
-//         read it), exponentiate, and write P (f16) over the row's S
+//         unloaded boxes zeroed; tile A's group for the V tiles tile A reads,
+//         tile B's for the rest), exponentiate, and write P (f16) over the
+//         row's S
 //   8     producer: finds the next item, TMA of its Q tiles, then 64-key K and
 //         V tiles into separate 4-stage rings: one copy per tile where the
 //         block size is a multiple of 64, else four 16-token boxes per tile
@@ -683,12 +684,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // of unloaded boxes zeroed (their weight is 0, and 0 * NaN would be
             // NaN).  Every softmax warp takes part in every V tile, in order: it
             // waits for the tile to land, converts its share and arrives once on
-            // the stage's v_conv (8 arrivals).  The share is half of the 16-byte
-            // chunks when both Q tiles read the V tile, all of them when only this
-            // group's tile does, none when only the other's does; so no group's
-            // parity wait on a V stage can fall two phases behind.  A group's share
-            // of V tile j is done right after it has loaded S of key tile j.
-            auto convert_v = [&](int jv, uint32_t vmask_bits, int mode) -> bool {
+            // the stage's v_conv (8 arrivals), so no group's parity wait on a V
+            // stage can fall two phases behind.  Tile A's group converts every V
+            // tile its tile reads, tile B's group only those tile A does not
+            // read: B's group, with less to do per key tile, then runs behind
+            // A's rather than in step with it, and the two tiles' MMAs queue
+            // less behind each other.  A group converts V tile j right after
+            // loading S of key tile j.
+            auto convert_v = [&](int jv, uint32_t vmask_bits, bool convert) -> bool {
                 const int gv = g0 + jv, sv = gv % kTcVStages, kb = jv * kTcKeys;
                 if (!__all_sync(FULL, mbar_wait(&v_full[sv], (gv / kTcVStages) & 1)))
                     return false;
@@ -697,7 +700,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // thread r owns 16-byte chunks r + 128 u (chunk i: half i / 512,
                 // key row (i / 8) % 64, one of the row's eight column groups)
                 constexpr int NCH = HALVES * kTcKeys * 8 / 128;
-                constexpr int NH = NCH / 2;
                 auto run = [&](int u0, auto nu_c) {
                     constexpr int NU = decltype(nu_c)::value;
                     uint4 w[NU];
@@ -727,9 +729,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int u = 0; u < NU; u++)
                         vt[r + 128 * (u0 + u)] = w[u];
                 };
-                if (mode == 1)
-                    run(tq * NH, std::integral_constant<int, NH>());
-                else if (mode == 2)
+                if (convert)
                     run(0, std::integral_constant<int, NCH>());
                 fence_proxy_async_smem();
                 tc::fence_before();  // also orders this warp's tcgen05.st of P
@@ -738,8 +738,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive(&v_conv[sv]);
                 return true;
             };
-            // this group's share of V tile jv (it reads V tiles 0 .. nkt - 1)
-            auto share = [&](int jv) { return jv >= nkt ? 0 : (jv < nk_other ? 1 : 2); };
+            // whether this group converts V tile jv (its tile reads V tiles
+            // 0 .. nkt - 1)
+            auto share = [&](int jv) { return jv < nkt && (tq == 0 || jv >= nk_other); };
             if (nkt > 0) {
                 // boxes of a tile the producer loads (block ids in [0, NB)); read
                 // from the table here, not from the producer, whose K stage may
@@ -878,7 +879,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // V tiles of this item that only the other Q tile reads: no share to
             // convert, but this group arrives on them in order too
             for (int jv = nkt; ok && jv < max(it.nkt[0], it.nkt[1]); jv++)
-                ok = convert_v(jv, 0xFu, 0);
+                ok = convert_v(jv, 0xFu, false);
             if (!ok)
                 break;
             if (nkt > 0) {
