@@ -217,19 +217,20 @@ pkv_status make_cache_map(CUtensorMap *map, const void *cache, long long tokens,
     return PKV_OK;
 }
 
-// The same cache for the prefill kernel's whole-tile copies, where a block
-// holds whole 64-token tiles (bs % 64 == 0): 4-D (64 columns, tokens, Hkv,
-// D/64 halves), box 64 x 64 x 1 x D/64, landing as the tile's halves one after
-// the other, each 64 rows of 128 B with the 128-byte swizzle (the layout the
-// score and P.V MMAs read).
-pkv_status make_cache_tile_map(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D)
+// The same cache for the prefill kernel's copies of both halves at once: 4-D
+// (64 columns, tokens, Hkv, D/64 halves), box 64 x rows x 1 x D/64, landing as
+// the halves one after the other, each `rows` rows of 128 B with the 128-byte
+// swizzle.  rows = 64: a whole K or V tile where a block holds whole 64-token
+// tiles (bs % 64 == 0); rows = 16: one 16-token box of a V tile.
+pkv_status make_cache_tile_map(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D,
+                               int rows)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc)
         return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[4] = {64, (cuuint64_t)tokens, (cuuint64_t)Hkv, (cuuint64_t)(D / 64)};
     cuuint64_t strides[3] = {(cuuint64_t)Hkv * D * 2, (cuuint64_t)D * 2, 128};
-    cuuint32_t box[4] = {64, (cuuint32_t)pkv::kPrefillKeys, 1, (cuuint32_t)(D / 64)};
+    cuuint32_t box[4] = {64, (cuuint32_t)rows, 1, (cuuint32_t)(D / 64)};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -281,9 +282,10 @@ pkv_status make_cache_map8(CUtensorMap *map, const void *cache, long long tokens
 
 // Tensor maps of recently used caches, per host thread (a map is plain data:
 // the same cache pointer and shape always encode the same map).
-// Map kinds: 16-token boxes of a bf16 cache, of an FP8 cache, or whole
-// 64-token prefill tiles of a bf16 cache.
-enum MapKind { kMapBox = 0, kMapBox8 = 1, kMapTile = 2 };
+// Map kinds: 16-token boxes of a bf16 cache (one half per copy), of an FP8
+// cache, or, for the prefill kernel, whole 64-token tiles or 16-token boxes
+// of a bf16 cache with both halves per copy.
+enum MapKind { kMapBox = 0, kMapBox8 = 1, kMapTile = 2, kMapBoxHalves = 3 };
 struct MapEntry {
     const void *ptr = nullptr;
     long long tokens = 0;
@@ -304,8 +306,9 @@ pkv_status cached_cache_map(CUtensorMap *map, const void *cache, long long token
             return PKV_OK;
         }
     const pkv_status ps = kind == kMapBox8   ? make_cache_map8(map, cache, tokens, Hkv, D)
-                          : kind == kMapTile ? make_cache_tile_map(map, cache, tokens, Hkv, D)
-                                             : make_cache_map(map, cache, tokens, Hkv, D);
+                          : kind == kMapTile ? make_cache_tile_map(map, cache, tokens, Hkv, D, pkv::kPrefillKeys)
+                          : kind == kMapBoxHalves ? make_cache_tile_map(map, cache, tokens, Hkv, D, pkv::kBox)
+                                                  : make_cache_map(map, cache, tokens, Hkv, D);
     if (ps != PKV_OK)
         return ps;
     MapEntry &e = t_maps[t_map_next];
@@ -647,13 +650,13 @@ pkv_status pkv_paged_prefill(const void *q, const void *k_cache, const void *v_c
     }
     CUtensorMap tmq, tmk, tmv;
     const long long tokens = (long long)NB * bs;
-    // blocks of whole 64-token tiles: one copy per K or V tile, else one per
-    // 16-token box and 64-column half
+    // blocks of whole 64-token tiles: one copy per K or V tile; else K one
+    // copy per 16-token box and 64-column half, V one per box
     const bool tile_copies = bs % pkv::kPrefillKeys == 0;
-    const int kind = tile_copies ? kMapTile : kMapBox;
-    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D, kind)) != PKV_OK)
+    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D, tile_copies ? kMapTile : kMapBox)) != PKV_OK)
         return ps;
-    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D, kind)) != PKV_OK)
+    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D, tile_copies ? kMapTile : kMapBoxHalves)) !=
+        PKV_OK)
         return ps;
     if ((ps = make_q_map(&tmq, q, Tq, Hq, D, G)) != PKV_OK)
         return ps;

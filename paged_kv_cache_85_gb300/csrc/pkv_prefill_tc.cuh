@@ -482,10 +482,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         mbar_arrive_expect_tx(&fb[s], (uint32_t)__popc(mask) * kBoxBytes);
                     __syncwarp();
                     if (loaded) {
+                        if (is_k) {
+                            // K: [half][64 rows], the layout the score MMA's
+                            // descriptor walks with one stride along the keys
 #pragma unroll
-                        for (int h = 0; h < HALVES; h++)
-                            tma_load_4d(dst + lane * (kBox * 128) + h * kTileHalf, map, 0, h, it.kvh, row,
-                                        &fb[s]);
+                            for (int h = 0; h < HALVES; h++)
+                                tma_load_4d(dst + lane * (kBox * 128) + h * kTileHalf, map, 0, h, it.kvh,
+                                            row, &fb[s]);
+                        } else {
+                            // V: one copy per box, both halves: [box][half][16 rows]
+                            tma_load_4d(dst + lane * kBoxBytes, map, 0, row, it.kvh, 0, &fb[s]);
+                        }
                     }
                 }
             };
@@ -553,6 +560,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t idS = tc::idesc_bf16(kTcRows, kTcKeys, false) | (p.neg_scale ? 1u << 13 : 0u);
         const uint32_t idO = tc::idesc_f16(kTcRows, D, true);
         const uint32_t dS0 = tmem + kTcSCol + 128u * (uint32_t)t, dO = tmem + 128u * (uint32_t)t;
+        // V tile layout: whole-tile copies land as [half][64 rows]; per-box
+        // copies as [16-token box][half][16 rows] (rows of 128 B).  A P.V MMA
+        // takes 16 keys: one box; its halves are v_lbo apart
+        const uint32_t v_lbo = p.tile_copies ? kTileHalf : (uint32_t)kBox * 128;
+        const uint32_t v_kstep = p.tile_copies ? 16u * 128 : (uint32_t)kBoxBytes;
         uint64_t *my_o_free = o_free(t);
         int g0 = 0;    // K/V tiles of the previous items
         int gq = 0;    // S/P tiles of this Q tile over the previous items
@@ -625,7 +637,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             {
 #pragma unroll
                                 for (int kk = 0; kk < kTcKeys / 16; kk++) {
-                                    const uint64_t dv = tc::smem_desc(va + kk * 16 * 128, kTileHalf, 1024);
+                                    const uint64_t dv = tc::smem_desc(va + kk * v_kstep, v_lbo, 1024);
                                     tc::mma_ts(dO, pP + 8 * kk, dv, idO, (jj > 0 || kk > 0) ? 1u : 0u);
                                 }
                                 tc::commit(smem_u32(pv_done(t, gp & 1)));
@@ -716,7 +728,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (vmask) {  // the same for the whole CTA: a tile with rows to clear
 #pragma unroll
                         for (int u = 0; u < NU; u++) {
-                            const int kr = ((r + 128 * (u0 + u)) / 8) % kTcKeys;
+                            const int ci = r + 128 * (u0 + u);  // 16-byte chunk
+                            const int kr = p.tile_copies ? (ci / 8) % kTcKeys
+                                                         : (ci / (8 * kBox * HALVES)) * kBox + (ci / 8) % kBox;
                             if (kb + kr >= k_len || !((vmask_bits >> (kr / kBox)) & 1u))
                                 w[u] = make_uint4(0u, 0u, 0u, 0u);
                         }
