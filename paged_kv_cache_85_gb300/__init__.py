@@ -110,13 +110,17 @@ def _check(status: int):
         raise PkvError(status, msg)
 
 
-def _require(t, name, dtype, ndim):
+def _require(t, name, dtype, ndim, host_ok=False):
+    """A contiguous tensor the kernels can address: CUDA memory or, where
+    ``host_ok`` (an output the kernels write once), pinned host memory."""
     import torch
 
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != dtype or t.dim() != ndim or not t.is_cuda or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor with {ndim} dims; "
+    addressable = t.is_cuda or (host_ok and t.device.type == "cpu" and t.is_pinned())
+    if t.dtype != dtype or t.dim() != ndim or not addressable or not t.is_contiguous():
+        where = "CUDA or pinned host" if host_ok else "CUDA"
+        raise ValueError(f"{name} must be a contiguous {where} {dtype} tensor with {ndim} dims; "
                          f"got {t.dtype}, shape {tuple(t.shape)}, device {t.device}, "
                          f"contiguous={t.is_contiguous()}")
 
@@ -191,7 +195,11 @@ def _workspace(device, stream_handle, nbytes):
 
 def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
                       max_ctas=0, workspace=None, err_flag=None):
-    """One decode step of paged attention; writes ``out`` in place and returns it."""
+    """One decode step of paged attention; writes ``out`` in place and returns it.
+
+    ``out`` may be a CUDA tensor or a pinned CPU tensor, which the kernels
+    then write directly over the host link.
+    """
     import torch
 
     _require(q, "q", torch.bfloat16, 3)
@@ -199,7 +207,7 @@ def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ou
     _require(v_cache, "v_cache", torch.bfloat16, 4)
     _require(block_tables, "block_tables", torch.int32, 2)
     _require(context_lens, "context_lens", torch.int32, 1)
-    _require(out, "out", torch.bfloat16, 3)
+    _require(out, "out", torch.bfloat16, 3, host_ok=True)
     B, Hq, D = q.shape
     NB, bs, Hkv, D2 = k_cache.shape
     if v_cache.shape != k_cache.shape or D2 != D:
@@ -274,7 +282,7 @@ def paged_attn_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale
     _require_fp8_cache(v_cache, "v_cache")
     _require(block_tables, "block_tables", torch.int32, 2)
     _require(context_lens, "context_lens", torch.int32, 1)
-    _require(out, "out", torch.bfloat16, 3)
+    _require(out, "out", torch.bfloat16, 3, host_ok=True)
     B, Hq, D = q.shape
     NB, bs, Hkv, D2 = k_cache.shape
     if v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape:
@@ -309,7 +317,9 @@ def paged_prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k,
     q / out are [Tq, Hq, D] bf16 (the sequences' new tokens, concatenated);
     cu_seqlens_q / cu_seqlens_k are int32 [B + 1] on the device; new token i
     of sequence b attends to context positions 0 .. k_len_b - q_len_b + i.
-    Store the new tokens' K/V first (``store_kvcache``).  Returns ``out``.
+    Store the new tokens' K/V first (``store_kvcache``).  ``out`` may be a
+    CUDA tensor or a pinned CPU tensor, which the kernel then writes directly
+    over the host link.  Returns ``out``.
     """
     import torch
 
@@ -319,7 +329,7 @@ def paged_prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k,
     _require(block_tables, "block_tables", torch.int32, 2)
     _require(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
     _require(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
-    _require(out, "out", torch.bfloat16, 3)
+    _require(out, "out", torch.bfloat16, 3, host_ok=True)
     Tq, Hq, D = q.shape
     NB, bs, Hkv, D2 = k_cache.shape
     if v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape:
