@@ -78,11 +78,11 @@ struct TcSmem {
     size_t q, kv, bars, items, slot, total;
 };
 
-// Barriers: q_full, q_empty, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+// Barriers: q_full[2], q_empty[2], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
 // v_conv[VS], then per Q tile: s_full[2], pv_ready[2], pv_done[2], o_free;
 // then item_ready[2], item_free[2], mma_done.
 constexpr int kTcTileBars = 7;
-constexpr int kTcBars = 2 + 2 * kTcKStages + 3 * kTcVStages + 2 * kTcTileBars + 2 + 2 + 1;
+constexpr int kTcBars = 4 + 2 * kTcKStages + 3 * kTcVStages + 2 * kTcTileBars + 2 + 2 + 1;
 
 __host__ __device__ inline TcSmem tc_smem_layout(int D)
 {
@@ -266,9 +266,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const TcSmem L = tc_smem_layout(D);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *q_full = bars;                       // the item's Q tiles landed
-    uint64_t *q_empty = q_full + 1;                // the item's last S completed: Q may be replaced
-    uint64_t *k_full = q_empty + 1;
+    uint64_t *q_full = bars;                       // [2] Q tile t of the item landed
+    uint64_t *q_empty = q_full + 2;                // [2] tile t's last S of the item completed
+    uint64_t *k_full = q_empty + 2;
     uint64_t *k_empty = k_full + kTcKStages;       // both tiles' S of the K tile completed
     uint64_t *v_full = k_empty + kTcKStages;
     uint64_t *v_empty = v_full + kTcVStages;       // both tiles' P.V of the V tile completed
@@ -294,8 +294,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     grid_launch_dependents();
     if (warp == kTcProducerWarp && lane == 0) {
         // the Q, K and V stages are released by both MMA warps (one arrival each)
-        mbar_init(q_full, 1);
-        mbar_init(q_empty, 2);
+        for (int t = 0; t < 2; t++) {
+            mbar_init(&q_full[t], 1);
+            mbar_init(&q_empty[t], 1);  // the tile's MMA warp
+        }
         for (int s = 0; s < kTcKStages; s++) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 2);
@@ -344,6 +346,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         grid_dependency_wait();  // K/V may have just been written by store_kvcache
         int gk = 0, gv = 0;      // K and V tiles issued so far (all items)
+        int q_loads[2] = {0, 0}; // Q tiles A and B loaded so far
         bool ok = true;
         int n = 0;               // items published
         int k = 0;               // walk rounds
@@ -403,18 +406,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_arrive(&item_ready[sl]);
             if (it.b < 0)
                 break;
-            // ---- Q tiles, after the previous item's last S
-            if (n >= 1 && !(ok = __all_sync(FULL, mbar_wait(q_empty, (n - 1) & 1))))
-                break;
-            if (lane == 0) {
-                const int nq = it.nkt[1] > 0 ? 2 : 1;
-                mbar_arrive_expect_tx(q_full, (uint32_t)nq * HALVES * kQHalf);
-                for (int t = 0; t < nq; t++)
+            // ---- Q tiles: tile t's once that tile's last S of the previous item
+            // has completed (q_empty[t], one commit per item): tile A's is
+            // usually done a key tile or two before tile B's.  Tile B's only
+            // where it has work.
+            for (int t = 0; t < (it.nkt[1] > 0 ? 2 : 1) && ok; t++) {
+                if (n >= 1 && !(ok = __all_sync(FULL, mbar_wait(&q_empty[t], (n - 1) & 1))))
+                    break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&q_full[t], HALVES * kQHalf);
 #pragma unroll
                     for (int h = 0; h < HALVES; h++)
                         tma_load_4d(sQ + t * kQTile + h * kQHalf, &tmq, 0, h, it.kvh * G,
-                                    it.cq0 + it.tok0 + t * TPC, q_full);
+                                    it.cq0 + it.tok0 + t * TPC, &q_full[t]);
+                }
+                ++q_loads[t];
             }
+            if (!ok)
+                break;
             n++;
             // ---- K and V tiles.  One converged loop serves both rings: it
             // probes (without blocking) whether the next K stage and the next
@@ -534,8 +543,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok)
                 flag_error(p.err_flag, 0x8 /* PKV_FLAG_TIMEOUT */);
             // copies still in flight land before the CTA may exit
-            if (n >= 1)
-                mbar_wait(q_full, (n - 1) & 1);
+            for (int t = 0; t < 2; t++)
+                if (q_loads[t] >= 1)
+                    mbar_wait(&q_full[t], (q_loads[t] - 1) & 1);
             for (int g = max(0, gk - kTcKStages); g < gk; g++)
                 mbar_wait(&k_full[g % kTcKStages], (g / kTcKStages) & 1);
             for (int g = max(0, gv - kTcVStages); g < gv; g++)
@@ -577,13 +587,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const PrefillItem it = items[n & 1];
                 if (it.b < 0)
                     break;
-                if (!(ok = mbar_wait(q_full, n & 1)))
-                    break;
-                tc::fence_after();
                 const int nk = it.nkt[t];
                 const int nkt = max(it.nkt[0], it.nkt[1]);
+                // this tile's Q of the item (loaded only where it has work)
+                if (nk > 0 && !(ok = mbar_wait(&q_full[t], used & 1)))
+                    break;
+                tc::fence_after();
                 if (nk == 0)
-                    tc::commit(smem_u32(q_empty));  // this tile reads no Q this item
+                    tc::commit(smem_u32(&q_empty[t]));  // this tile reads no Q this item
                 for (int j = 0; j <= nkt && ok; j++) {
                     if (j < nkt) {
                         const int gkt = g0 + j, s = gkt % kTcKStages;
@@ -611,7 +622,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 tc::commit(smem_u32(s_full(t, gs & 1)));
                                 tc::commit(smem_u32(&k_empty[s]));
                                 if (j == nk - 1)
-                                    tc::commit(smem_u32(q_empty));
+                                    tc::commit(smem_u32(&q_empty[t]));
                             }
                         } else {
                             tc::commit(smem_u32(&k_empty[s]));  // a K tile this Q tile does not read
