@@ -263,7 +263,11 @@ pkv_status pkv_store_kvcache_fp8(const void *k, const void *v, void *k_cache, vo
  *   - P.V in f16: V codes converted to f16 (exact), P rounded to f16;
  *   - output rounded to bf16.
  * Three CTAs of four workers run per SM (one CTA of eight where they do not
- * fit).
+ * fit).  Where those CTAs would hold fewer than four pipeline stages of
+ * 16-token boxes (large B or G) and bs is a multiple of 32, the streams are
+ * cut into 32-token boxes instead (two stages), which halves the per-box
+ * work for the same bytes in flight; the results agree within the
+ * tolerance above, not bit for bit, with a 16-token split.
  */
 pkv_status pkv_paged_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
                                      const int32_t *block_tables, int MBS,

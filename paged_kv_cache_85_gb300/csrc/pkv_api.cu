@@ -29,10 +29,10 @@ PKV_DECLARE_SHAPE(128, 4)
 PKV_DECLARE_SHAPE(128, 8)
 #undef PKV_DECLARE_SHAPE
 #define PKV_DECLARE_SHAPE8(D, NW)                                                                 \
-    cudaError_t launch_decode8_d##D##_w##NW(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,\
-                                            const DecodeParams &p, int grid, size_t smem,         \
-                                            cudaStream_t stream);                                 \
-    const void *decode_kernel8_d##D##_w##NW(int G);
+    cudaError_t launch_decode8_d##D##_w##NW(int G, int bt, const CUtensorMap *tmk,                \
+                                            const CUtensorMap *tmv, const DecodeParams &p,        \
+                                            int grid, size_t smem, cudaStream_t stream);          \
+    const void *decode_kernel8_d##D##_w##NW(int G, int bt);
 PKV_DECLARE_SHAPE8(64, 4)
 PKV_DECLARE_SHAPE8(64, 8)
 PKV_DECLARE_SHAPE8(128, 4)
@@ -62,30 +62,31 @@ const void *prefill_kernel(int D, int G)
 
 size_t prefill_smem_bytes(int D) { return tc_smem_layout(D).total; }
 
-const void *decode_kernel(int D, int NW, int G, bool f8)
+// bt: tokens per box (16, or 32 for FP8 caches with block sizes divisible by 32)
+const void *decode_kernel(int D, int NW, int G, bool f8, int bt)
 {
     const bool pair = NW == kPairWorkers;
     if (f8) {
         if (D == 128)
-            return pair ? decode_kernel8_d128_w4(G) : decode_kernel8_d128_w8(G);
-        return pair ? decode_kernel8_d64_w4(G) : decode_kernel8_d64_w8(G);
+            return pair ? decode_kernel8_d128_w4(G, bt) : decode_kernel8_d128_w8(G, bt);
+        return pair ? decode_kernel8_d64_w4(G, bt) : decode_kernel8_d64_w8(G, bt);
     }
     if (D == 128)
         return pair ? decode_kernel_d128_w4(G) : decode_kernel_d128_w8(G);
     return pair ? decode_kernel_d64_w4(G) : decode_kernel_d64_w8(G);
 }
 
-cudaError_t launch_decode(int D, int NW, int G, bool f8, const CUtensorMap *tmk,
+cudaError_t launch_decode(int D, int NW, int G, bool f8, int bt, const CUtensorMap *tmk,
                           const CUtensorMap *tmv, const DecodeParams &p, int grid, size_t smem,
                           cudaStream_t stream)
 {
     const bool pair = NW == kPairWorkers;
     if (f8) {
         if (D == 128)
-            return pair ? launch_decode8_d128_w4(G, tmk, tmv, p, grid, smem, stream)
-                        : launch_decode8_d128_w8(G, tmk, tmv, p, grid, smem, stream);
-        return pair ? launch_decode8_d64_w4(G, tmk, tmv, p, grid, smem, stream)
-                    : launch_decode8_d64_w8(G, tmk, tmv, p, grid, smem, stream);
+            return pair ? launch_decode8_d128_w4(G, bt, tmk, tmv, p, grid, smem, stream)
+                        : launch_decode8_d128_w8(G, bt, tmk, tmv, p, grid, smem, stream);
+        return pair ? launch_decode8_d64_w4(G, bt, tmk, tmv, p, grid, smem, stream)
+                    : launch_decode8_d64_w8(G, bt, tmk, tmv, p, grid, smem, stream);
     }
     if (D == 128)
         return pair ? launch_decode_d128_w4(G, tmk, tmv, p, grid, smem, stream)
@@ -120,7 +121,7 @@ struct DeviceState {
     bool ready = false;
     int dev = 0;
     int sms = 0;
-    bool smem_set[2][2][2][9] = {};  // [fp8][D == 128][NW == 8][G]
+    bool smem_set[2][2][2][2][9] = {};  // [fp8][32-token boxes][D == 128][NW == 8][G]
     bool pf_smem_set[2][9] = {};     // prefill: [D == 128][G]
 };
 DeviceState g_dev[kMaxDevices];
@@ -260,16 +261,17 @@ pkv_status make_q_map(CUtensorMap *map, const void *q, long long Tq, int Hq, int
 }
 
 // FP8 cache [NB*bs tokens, Hkv, D] as bytes: 3-D (D, Hkv, tokens), box
-// D x 1 x 16, swizzled at the row width (128-byte rows for D = 128, 64-byte
-// rows for D = 64).
-pkv_status make_cache_map8(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D)
+// D x 1 x rows (16 or 32 tokens), swizzled at the row width (128-byte rows
+// for D = 128, 64-byte rows for D = 64).
+pkv_status make_cache_map8(CUtensorMap *map, const void *cache, long long tokens, int Hkv, int D,
+                           int rows)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc)
         return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)tokens};
     cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)Hkv * D};
-    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)pkv::kBox};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(cache), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -282,10 +284,10 @@ pkv_status make_cache_map8(CUtensorMap *map, const void *cache, long long tokens
 
 // Tensor maps of recently used caches, per host thread (a map is plain data:
 // the same cache pointer and shape always encode the same map).
-// Map kinds: 16-token boxes of a bf16 cache (one half per copy), of an FP8
-// cache, or, for the prefill kernel, whole 64-token tiles or 16-token boxes
-// of a bf16 cache with both halves per copy.
-enum MapKind { kMapBox = 0, kMapBox8 = 1, kMapTile = 2, kMapBoxHalves = 3 };
+// Map kinds: 16-token boxes of a bf16 cache (one half per copy), 16- or
+// 32-token boxes of an FP8 cache, or, for the prefill kernel, whole 64-token
+// tiles or 16-token boxes of a bf16 cache with both halves per copy.
+enum MapKind { kMapBox = 0, kMapBox8 = 1, kMapTile = 2, kMapBoxHalves = 3, kMapBox8Wide = 4 };
 struct MapEntry {
     const void *ptr = nullptr;
     long long tokens = 0;
@@ -305,7 +307,8 @@ pkv_status cached_cache_map(CUtensorMap *map, const void *cache, long long token
             *map = e.map;
             return PKV_OK;
         }
-    const pkv_status ps = kind == kMapBox8   ? make_cache_map8(map, cache, tokens, Hkv, D)
+    const pkv_status ps = kind == kMapBox8   ? make_cache_map8(map, cache, tokens, Hkv, D, pkv::kBox)
+                          : kind == kMapBox8Wide ? make_cache_map8(map, cache, tokens, Hkv, D, 2 * pkv::kBox)
                           : kind == kMapTile ? make_cache_tile_map(map, cache, tokens, Hkv, D, pkv::kPrefillKeys)
                           : kind == kMapBoxHalves ? make_cache_tile_map(map, cache, tokens, Hkv, D, pkv::kBox)
                                                   : make_cache_map(map, cache, tokens, Hkv, D);
@@ -327,6 +330,7 @@ pkv_status cached_cache_map(CUtensorMap *map, const void *cache, long long token
 // always agree.
 struct DecodePlan {
     int G = 0, NW = 0, stages = 0, grid = 0;
+    int bt = pkv::kBox;  // tokens per box
     size_t smem = 0, hdr_bytes = 0, ws_bytes = 0;
     const void *kernel = nullptr;
 };
@@ -364,11 +368,27 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
     const int eb = f8 ? 1 : 2;  // bytes per cached element
     int NW = pkv::kPairWorkers;
     int stages = 0;
-    if (f8)
+    int bt = pkv::kBox;
+    if (f8) {
         stages = pkv::decode_stages_for(D, G, NW, B, pkv::kMaxStages, trio_smem, eb);
-    if (stages < pkv::kPairStages)
+        // Where three CTAs per SM hold fewer than four stages of 16-token
+        // boxes (large B or G), and the blocks hold whole 32-token boxes, two
+        // stages of 32-token boxes keep as many bytes in flight while one is
+        // consumed, with half the boxes (stage waits, descriptors, softmax
+        // reductions) per byte.  With four 16-token stages the deeper ring
+        // wins (measured).
+        if (stages < pkv::kMaxStages && bs % (2 * pkv::kBox) == 0) {
+            const int s32 = pkv::decode_stages_for(D, G, NW, B, pkv::kMaxStages, trio_smem, eb,
+                                                   2 * pkv::kBox);
+            if (s32 >= pkv::kMinStages) {
+                bt = 2 * pkv::kBox;
+                stages = s32;
+            }
+        }
+    }
+    if (bt == pkv::kBox && stages < pkv::kPairStages)
         stages = pkv::decode_stages_for(D, G, NW, B, pkv::kPairStages, pair_smem, eb);
-    if (stages < pkv::kPairStages) {
+    if (bt == pkv::kBox && stages < pkv::kPairStages) {
         NW = pkv::kWideWorkers;
         stages = pkv::decode_stages_for(D, G, NW, B, pkv::kMaxStages, kMaxDynSmem, eb);
     }
@@ -394,7 +414,8 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
     plan->G = G;
     plan->NW = NW;
     plan->stages = stages;
-    plan->smem = pkv::decode_smem_layout(D, G, NW, stages, B, eb).total;
+    plan->bt = bt;
+    plan->smem = pkv::decode_smem_layout(D, G, NW, stages, B, eb, bt).total;
     plan->hdr_bytes = pkv::align_up((size_t)(pkv::kWsHeaderInts + B + 1) * 4, 256);
     plan->ws_bytes = plan->hdr_bytes +
                      (size_t)workers_cap * 2 * G * (size_t)(D + 4) * sizeof(float);
@@ -405,10 +426,10 @@ pkv_status plan_decode(int B, int Hq, int Hkv, int D, int MBS, int bs, int max_c
     pkv_status ps = device_state(&st);
     if (ps != PKV_OK)
         return ps;
-    const void *kfn = pkv::decode_kernel(D, NW, G, f8);
+    const void *kfn = pkv::decode_kernel(D, NW, G, f8, bt);
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        bool &set = st->smem_set[f8][D == 128][NW == pkv::kWideWorkers][G];
+        bool &set = st->smem_set[f8][bt != pkv::kBox][D == 128][NW == pkv::kWideWorkers][G];
         if (!set) {
             cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)kMaxDynSmem);
@@ -477,9 +498,10 @@ static pkv_status decode_impl(const void *q, const void *k_cache, const void *v_
 
     CUtensorMap tmk, tmv;
     const long long tokens = (long long)NB * bs;
-    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D, f8 ? kMapBox8 : kMapBox)) != PKV_OK)
+    const int kind = !f8 ? kMapBox : plan.bt == pkv::kBox ? kMapBox8 : kMapBox8Wide;
+    if ((ps = cached_cache_map(&tmk, k_cache, tokens, Hkv, D, kind)) != PKV_OK)
         return ps;
-    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D, f8 ? kMapBox8 : kMapBox)) != PKV_OK)
+    if ((ps = cached_cache_map(&tmv, v_cache, tokens, Hkv, D, kind)) != PKV_OK)
         return ps;
 
     pkv::DecodeParams p;
@@ -501,7 +523,8 @@ static pkv_status decode_impl(const void *q, const void *k_cache, const void *v_
     p.v_scale = f8 ? v_scale : 1.f;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = pkv::launch_decode(D, plan.NW, plan.G, f8, &tmk, &tmv, p, plan.grid, plan.smem, s);
+    cudaError_t e = pkv::launch_decode(D, plan.NW, plan.G, f8, plan.bt, &tmk, &tmv, p, plan.grid,
+                                       plan.smem, s);
     if (e != cudaSuccess)
         return fail(PKV_ERR_CUDA, "paged_attn_decode launch: %s", cudaGetErrorString(e));
     e = pkv::launch_merge(D, plan.G, p, s);

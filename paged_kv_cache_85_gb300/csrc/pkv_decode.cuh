@@ -9,7 +9,9 @@
 //
 // How (GB300 design):
 //  * Work decomposition (stream-K).  Each (sequence, KV head) context is a
-//    stream of 16-token boxes; all G query heads of the group ride along, so
+//    stream of 16-token boxes (32-token boxes for FP8 caches where three
+//    CTAs per SM hold fewer than four 16-token stages and whole 32-token
+//    boxes fit in a block); all G query heads of the group ride along, so
 //    every K/V byte is read from HBM once.  The streams are concatenated
 //    (KV-head-major); each head's region is cut into equal contiguous
 //    slices, one per worker, so the workers of different heads read the
@@ -72,12 +74,13 @@ struct DecodeSmem {
 
 
 __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int NW, int stages, int B,
-                                                         int kv_elem_bytes = 2)
+                                                         int kv_elem_bytes = 2, int box_tokens = kBox)
 {
     DecodeSmem L;
     size_t o = 0;
-    L.kv = o;  // per stage: K boxes [NW][D/64][16][64], then V boxes alike (128B-swizzled rows)
-    o += (size_t)stages * 2 * NW * kBox * D * kv_elem_bytes;
+    L.kv = o;  // per stage: K boxes [NW][D/64][16][64], then V boxes alike (128B-swizzled rows);
+               // FP8 boxes [NW][box_tokens][D]
+    o += (size_t)stages * 2 * NW * box_tokens * D * kv_elem_bytes;
     L.q = o;  // per stage and worker: G query rows
     o = align_up(o + (size_t)stages * NW * G * D * 2, 16);
     L.full = o;
@@ -98,10 +101,10 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int G, int NW, i
 
 // Deepest pipeline (2..max_stages) whose shared memory fits max_smem.
 inline int decode_stages_for(int D, int G, int NW, int B, int max_stages, size_t max_smem,
-                             int kv_elem_bytes = 2)
+                             int kv_elem_bytes = 2, int box_tokens = kBox)
 {
     for (int s = max_stages; s >= kMinStages; s--)
-        if (decode_smem_layout(D, G, NW, s, B, kv_elem_bytes).total <= max_smem)
+        if (decode_smem_layout(D, G, NW, s, B, kv_elem_bytes, box_tokens).total <= max_smem)
             return s;
     return 0;
 }
@@ -145,9 +148,10 @@ __device__ __forceinline__ void next_box(const int *pb, int B, int &b, int &h, i
     }
 }
 
+template <int BT>
 __device__ __forceinline__ int box_block(const DecodeParams &p, int b, int j)
 {
-    return __ldg(p.block_tables + (size_t)b * p.MBS + (j * kBox) / p.bs);
+    return __ldg(p.block_tables + (size_t)b * p.MBS + (j * BT) / p.bs);
 }
 
 // Producer warp: lane w < NW runs worker w of this CTA.  Each lane
@@ -156,14 +160,14 @@ __device__ __forceinline__ int box_block(const DecodeParams &p, int b, int j)
 // register queue, so a copy never waits on a block-table read.  Per stage
 // every lane writes its worker's box descriptor and issues its own TMA
 // copies; lane 0 arms the stage's mbarrier with the summed byte count.
-template <int D, int G, int NW, bool F8>
+template <int D, int G, int NW, bool F8, int BT>
 __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CUtensorMap *tmv,
                                                 const DecodeParams &p, uint8_t *smem,
                                                 const DecodeSmem &L, int lane, int R, int Tr,
                                                 int Wr, int P)
 {
     constexpr unsigned FULL = 0xffffffffu;
-    constexpr int kBoxBytes = kBox * D * (F8 ? 1 : 2);
+    constexpr int kBoxBytes = BT * D * (F8 ? 1 : 2);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
     BoxMeta *meta = reinterpret_cast<BoxMeta *>(smem + L.meta);
@@ -194,7 +198,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
     for (int i = 0; i < kLookahead; i++) {
         qb[i] = -1;
         if (lpos < end) {
-            qb[i] = box_block(p, lb, lj);
+            qb[i] = box_block<BT>(p, lb, lj);
             next_box(pb, p.B, lb, lh, lj);
         }
         ++lpos;
@@ -229,7 +233,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
             const int j = cj;
             const int blk = qb[u];
             const int nb = pb[b + 1] - pb[b];
-            const int tok0 = j * kBox;
+            const int tok0 = j * BT;
             const bool loaded = blk >= 0 && blk < p.NB;
             if (!loaded)
                 flag_error(p.err_flag, 0x2 /* PKV_FLAG_BAD_BLOCK */);
@@ -246,7 +250,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
             m.b = b;
             m.h = h;
             m.tok0 = tok0;
-            m.nvalid = min(kBox, len[b] - tok0);
+            m.nvalid = min(BT, len[b] - tok0);
             m.flags = flags;
             m.blk = blk;
             // advance both cursors
@@ -254,7 +258,7 @@ __device__ __forceinline__ void decode_producer(const CUtensorMap *tmk, const CU
             ++pos;
             qb[u] = -1;
             if (lpos < end) {
-                qb[u] = box_block(p, lb, lj);
+                qb[u] = box_block<BT>(p, lb, lj);
                 next_box(pb, p.B, lb, lh, lj);
             }
             ++lpos;
@@ -496,7 +500,9 @@ template <int D> __device__ __forceinline__ uint32_t box8_chunk(int t, int c)
 }
 
 // Consumer warp for FP8 (E4M3) caches.  Same pipeline, slices and outputs as
-// the bf16 consumer; the arithmetic is arranged around the 8-bit data:
+// the bf16 consumer; a box of BT = 16 or 32 tokens is taken as BT / 16
+// sub-boxes of 16 tokens (one MMA tile each) under one online-softmax update.
+// The arithmetic is arranged around the 8-bit data:
 //   * scores S^T = K q^T run on the E4M3 tensor-core path (m16n8k32) with the
 //     box's 16 tokens as M and the group's heads as N, so K fragments are
 //     the raw codes read from shared memory, four per 32-bit word.  q enters
@@ -514,7 +520,7 @@ template <int D> __device__ __forceinline__ uint32_t box8_chunk(int t, int c)
 //     max exceeds it by more than 2^8, which bounds P by 256 (exact range of
 //     f16) and skips the rescale on most boxes.
 // k_scale is folded into the score scale and v_scale into the output.
-template <int D, int G, int NW>
+template <int D, int G, int NW, int BT>
 __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8_t *smem,
                                                     const DecodeSmem &L, int warp, int lane)
 {
@@ -522,7 +528,8 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8
     constexpr int KW = D / 16;   // K words per lane per token row (D/4 bytes)
     constexpr int MT = D / 16;   // m-tiles of O^T
     constexpr int VW = D / 32;   // V words per lane per token row (D/8 bytes)
-    constexpr int kBoxBytes = kBox * D;
+    constexpr int NSUB = BT / 16; // 16-token sub-boxes per box (one MMA M tile each)
+    constexpr int kBoxBytes = BT * D;
     constexpr unsigned FULL = 0xffffffffu;
     constexpr float kLazy = 8.f;
 
@@ -632,55 +639,84 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8
         if (nvw > 0) {
             const uint8_t *Ks = smem + L.kv + ((size_t)stage * 2 * NW + warp) * kBoxBytes;
             const uint8_t *Vs = Ks + (size_t)NW * kBoxBytes;
-            // ---- scores S^T (tokens g, g+8; heads h0, h1) ----
-            uint32_t ka[2][KW];
+            // ---- scores S^T (tokens g, g+8 of each 16-token sub-box; heads h0, h1) ----
+            // sub-box u holds tokens 16u .. 16u+15 of the box, 16 D bytes further
+            // on (the swizzle pattern repeats every 8 rows)
+            float sv[NSUB][4];
+            uint32_t vw[NSUB][4][VW];  // V words of tokens 2quad, 2quad+1, 2quad+8, 2quad+9
+            auto load_v = [&](int u, int nv) {
+                const uint8_t *Vu = Vs + u * 16 * D;
 #pragma unroll
-            for (int r = 0; r < 2; r++)
-#pragma unroll
-                for (int c = 0; c < KW / 4; c++) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(Ks + koff[r][c]);
-                    ka[r][4 * c + 0] = w.x;
-                    ka[r][4 * c + 1] = w.y;
-                    ka[r][4 * c + 2] = w.z;
-                    ka[r][4 * c + 3] = w.w;
-                }
-            float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int k = 0; k < KS; k++) {
-                mma_e4m3_16832(sh, ka[0][2 * k], ka[1][2 * k], ka[0][2 * k + 1], ka[1][2 * k + 1],
-                               qh[2 * k], qh[2 * k + 1]);
-                mma_e4m3_16832(sl, ka[0][2 * k], ka[1][2 * k], ka[0][2 * k + 1], ka[1][2 * k + 1],
-                               ql[2 * k], ql[2 * k + 1]);
-            }
-            float sv[4] = {fmaf(sl[0], f0l, sh[0] * f0), fmaf(sl[1], f1l, sh[1] * f1),
-                           fmaf(sl[2], f0l, sh[2] * f0), fmaf(sl[3], f1l, sh[3] * f1)};
-            // V words of tokens 2quad, 2quad+1, 2quad+8, 2quad+9
-            uint32_t vw[4][VW];
-#pragma unroll
-            for (int r = 0; r < 4; r++) {
-                if constexpr (VW == 4) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(Vs + voff[r]);
-                    vw[r][0] = w.x; vw[r][1] = w.y; vw[r][2] = w.z; vw[r][3] = w.w;
-                } else {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(Vs + voff[r]);
-                    vw[r][0] = w.x; vw[r][1] = w.y;
-                }
-            }
-            if (nvw < kBox) {
-                // tokens past the context: scores -inf, V 0 (0 * NaN is NaN)
-                if (g >= nvw) { sv[0] = -INFINITY; sv[1] = -INFINITY; }
-                if (g + 8 >= nvw) { sv[2] = -INFINITY; sv[3] = -INFINITY; }
-                const int rows[4] = {h0, h1, h0 + 8, h1 + 8};
-#pragma unroll
-                for (int r = 0; r < 4; r++)
-                    if (rows[r] >= nvw) {
-#pragma unroll
-                        for (int w = 0; w < VW; w++)
-                            vw[r][w] = 0u;
+                for (int r = 0; r < 4; r++) {
+                    if constexpr (VW == 4) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(Vu + voff[r]);
+                        vw[u][r][0] = w.x; vw[u][r][1] = w.y; vw[u][r][2] = w.z; vw[u][r][3] = w.w;
+                    } else {
+                        const uint2 w = *reinterpret_cast<const uint2 *>(Vu + voff[r]);
+                        vw[u][r][0] = w.x; vw[u][r][1] = w.y;
                     }
+                }
+                if (nv < 16) {
+                    // V of tokens past the context: 0 (0 * NaN is NaN)
+                    const int rows[4] = {h0, h1, h0 + 8, h1 + 8};
+#pragma unroll
+                    for (int r = 0; r < 4; r++)
+                        if (rows[r] >= nv) {
+#pragma unroll
+                            for (int w = 0; w < VW; w++)
+                                vw[u][r][w] = 0u;
+                        }
+                }
+            };
+#pragma unroll
+            for (int u = 0; u < NSUB; u++) {
+                const int nv = nvw - 16 * u;  // valid tokens of the sub-box (warp-uniform)
+                if (u > 0 && nv <= 0) {
+                    sv[u][0] = sv[u][1] = sv[u][2] = sv[u][3] = -INFINITY;
+                    continue;
+                }
+                const uint8_t *Ku = Ks + u * 16 * D;
+                uint32_t ka[2][KW];
+#pragma unroll
+                for (int r = 0; r < 2; r++)
+#pragma unroll
+                    for (int c = 0; c < KW / 4; c++) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(Ku + koff[r][c]);
+                        ka[r][4 * c + 0] = w.x;
+                        ka[r][4 * c + 1] = w.y;
+                        ka[r][4 * c + 2] = w.z;
+                        ka[r][4 * c + 3] = w.w;
+                    }
+                float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < KS; k++) {
+                    mma_e4m3_16832(sh, ka[0][2 * k], ka[1][2 * k], ka[0][2 * k + 1], ka[1][2 * k + 1],
+                                   qh[2 * k], qh[2 * k + 1]);
+                    mma_e4m3_16832(sl, ka[0][2 * k], ka[1][2 * k], ka[0][2 * k + 1], ka[1][2 * k + 1],
+                                   ql[2 * k], ql[2 * k + 1]);
+                }
+                sv[u][0] = fmaf(sl[0], f0l, sh[0] * f0);
+                sv[u][1] = fmaf(sl[1], f1l, sh[1] * f1);
+                sv[u][2] = fmaf(sl[2], f0l, sh[2] * f0);
+                sv[u][3] = fmaf(sl[3], f1l, sh[3] * f1);
+                // with one sub-box, its V words are loaded before the softmax,
+                // whose reductions cover their latency; with two, each after it
+                // (registers)
+                if (NSUB == 1)
+                    load_v(u, nv);
+                if (nv < 16) {
+                    // tokens past the context: scores -inf
+                    if (g >= nv) { sv[u][0] = -INFINITY; sv[u][1] = -INFINITY; }
+                    if (g + 8 >= nv) { sv[u][2] = -INFINITY; sv[u][3] = -INFINITY; }
+                }
             }
             // ---- online softmax per head column (log2 domain) ----
-            float b0 = fmaxf(sv[0], sv[2]), b1 = fmaxf(sv[1], sv[3]);
+            float b0 = fmaxf(sv[0][0], sv[0][2]), b1 = fmaxf(sv[0][1], sv[0][3]);
+#pragma unroll
+            for (int u = 1; u < NSUB; u++) {
+                b0 = fmaxf(b0, fmaxf(sv[u][0], sv[u][2]));
+                b1 = fmaxf(b1, fmaxf(sv[u][1], sv[u][3]));
+            }
 #pragma unroll
             for (int x = 4; x < 32; x <<= 1) {
                 b0 = fmaxf(b0, __shfl_xor_sync(FULL, b0, x));
@@ -701,22 +737,30 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8
                     o[j][3] *= a1;
                 }
             }
-            const float p0 = fast_exp2(sv[0] - m0), p1 = fast_exp2(sv[1] - m1);
-            const float p2 = fast_exp2(sv[2] - m0), p3 = fast_exp2(sv[3] - m1);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
-            const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
-            // ---- O^T += V^T P^T ----
 #pragma unroll
-            for (int w = 0; w < VW; w++) {
-                uint32_t a[2][4];  // [m-tile 2w + i][a0..a3]
+            for (int u = 0; u < NSUB; u++) {
+                const int nv = nvw - 16 * u;
+                if (u > 0 && nv <= 0)
+                    continue;  // no valid token: every weight is 0
+                const float p0 = fast_exp2(sv[u][0] - m0), p1 = fast_exp2(sv[u][1] - m1);
+                const float p2 = fast_exp2(sv[u][2] - m0), p3 = fast_exp2(sv[u][3] - m1);
+                l0 += p0 + p2;
+                l1 += p1 + p3;
+                const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
+                const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
+                if (NSUB > 1)
+                    load_v(u, nv);
+                // ---- O^T += V^T P^T ----
 #pragma unroll
-                for (int i = 0; i < 2; i++) {
-                    const uint32_t sel = i == 0 ? 0x5140u : 0x7362u;
-                    e4m3x4_to_f16x2x2(prmt(vw[0][w], vw[1][w], sel), a[i][0], a[i][1]);
-                    e4m3x4_to_f16x2x2(prmt(vw[2][w], vw[3][w], sel), a[i][2], a[i][3]);
-                    mma_f16_16816(o[2 * w + i], a[i][0], a[i][1], a[i][2], a[i][3], pb0, pb1);
+                for (int w = 0; w < VW; w++) {
+                    uint32_t a[2][4];  // [m-tile 2w + i][a0..a3]
+#pragma unroll
+                    for (int i = 0; i < 2; i++) {
+                        const uint32_t sel = i == 0 ? 0x5140u : 0x7362u;
+                        e4m3x4_to_f16x2x2(prmt(vw[u][0][w], vw[u][1][w], sel), a[i][0], a[i][1]);
+                        e4m3x4_to_f16x2x2(prmt(vw[u][2][w], vw[u][3][w], sel), a[i][2], a[i][3]);
+                        mma_f16_16816(o[2 * w + i], a[i][0], a[i][1], a[i][2], a[i][3], pb0, pb1);
+                    }
                 }
             }
         }
@@ -780,7 +824,8 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8
 }
 
 // Per-sequence clamped lengths and the exclusive prefix sum of their box
-// counts (boxes per KV head before sequence b), b = 0..B.
+// counts (boxes of BT tokens per KV head before sequence b), b = 0..B.
+template <int BT>
 __device__ __forceinline__ void build_prefix(const DecodeParams &p, int *pb, int *len, int *wsum)
 {
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -797,7 +842,7 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int *pb, int
             n = n < 0 ? 0 : maxctx;
         }
         len[b] = n;
-        local += (n + kBox - 1) / kBox;
+        local += (n + BT - 1) / BT;
     }
     if (bad && blockIdx.x == 0)
         flag_error(p.err_flag, 0x4 /* PKV_FLAG_BAD_CONTEXT_LEN */);
@@ -824,21 +869,24 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int *pb, int
     int run = wsum[warp] + incl - local;
     for (int b = lo; b < hi; b++) {
         pb[b] = run;
-        run += (len[b] + kBox - 1) / kBox;
+        run += (len[b] + BT - 1) / BT;
     }
     if (tid == 0)
         pb[p.B] = wsum[nt / 32];
     __syncthreads();
 }
 
-template <int D, int G, int NW, bool F8>
+// BT: tokens per box (16; 32 for FP8 caches whose block size is a multiple
+// of 32, which halves the per-box work of the producer and the consumers).
+template <int D, int G, int NW, bool F8, int BT>
 __global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? (F8 ? 3 : 2) : 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeParams p)
 {
+    static_assert(BT == kBox || (F8 && BT == 2 * kBox), "32-token boxes on the FP8 path only");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const DecodeSmem L = decode_smem_layout(D, G, NW, p.stages, p.B, F8 ? 1 : 2);
+    const DecodeSmem L = decode_smem_layout(D, G, NW, p.stages, p.B, F8 ? 1 : 2, BT);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -856,7 +904,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? (F8 ? 3 : 
     }
     int *pb = reinterpret_cast<int *>(smem + L.pb);
     int *len = reinterpret_cast<int *>(smem + L.len);
-    build_prefix(p, pb, len, reinterpret_cast<int *>(smem + L.scan));  // ends with __syncthreads()
+    build_prefix<BT>(p, pb, len, reinterpret_cast<int *>(smem + L.scan));  // ends with __syncthreads()
 
     // Slicing: with at least one worker per KV head, each head's region of
     // the concatenated streams gets W / Hkv workers and is cut on its own, so
@@ -869,7 +917,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? (F8 ? 3 : 
     const int P = Tr > 0 ? (Tr + Wr - 1) / Wr : 1;
 
     if (warp == NW) {
-        decode_producer<D, G, NW, F8>(&tmk, &tmv, p, smem, L, lane, R, Tr, Wr, P);
+        decode_producer<D, G, NW, F8, BT>(&tmk, &tmv, p, smem, L, lane, R, Tr, Wr, P);
     } else {
         if (blockIdx.x == 0) {
             // Publish the box layout for the merge kernel (after the previous
@@ -886,13 +934,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kPairWorkers ? (F8 ? 3 : 
             }
         }
         if constexpr (F8)
-            decode_consumer_fp8<D, G, NW>(p, smem, L, warp, lane);
+            decode_consumer_fp8<D, G, NW, BT>(p, smem, L, warp, lane);
         else
             decode_consumer<D, G, NW>(p, smem, L, warp, lane);
     }
 }
 
-template <int D, int NW, bool F8>
+template <int D, int NW, bool F8, int BT = kBox>
 inline cudaError_t launch_decode_shape(int G, const CUtensorMap *tmk, const CUtensorMap *tmv,
                                        const DecodeParams &p, int grid, size_t smem,
                                        cudaStream_t stream)
@@ -908,21 +956,21 @@ inline cudaError_t launch_decode_shape(int G, const CUtensorMap *tmk, const CUte
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     switch (G) {
-    case 1: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 1, NW, F8>, *tmk, *tmv, p);
-    case 2: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 2, NW, F8>, *tmk, *tmv, p);
-    case 4: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 4, NW, F8>, *tmk, *tmv, p);
-    case 8: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 8, NW, F8>, *tmk, *tmv, p);
+    case 1: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 1, NW, F8, BT>, *tmk, *tmv, p);
+    case 2: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 2, NW, F8, BT>, *tmk, *tmv, p);
+    case 4: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 4, NW, F8, BT>, *tmk, *tmv, p);
+    case 8: return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, 8, NW, F8, BT>, *tmk, *tmv, p);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int D, int NW, bool F8> inline const void *decode_kernel_shape(int G)
+template <int D, int NW, bool F8, int BT = kBox> inline const void *decode_kernel_shape(int G)
 {
     switch (G) {
-    case 1: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 1, NW, F8>);
-    case 2: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 2, NW, F8>);
-    case 4: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 4, NW, F8>);
-    case 8: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 8, NW, F8>);
+    case 1: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 1, NW, F8, BT>);
+    case 2: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 2, NW, F8, BT>);
+    case 4: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 4, NW, F8, BT>);
+    case 8: return reinterpret_cast<const void *>(&paged_decode_kernel<D, 8, NW, F8, BT>);
     default: return nullptr;
     }
 }

@@ -179,7 +179,7 @@ def test_grid_size_invariance_tiny(pkv, ctas):
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("bs", [16, 48, 256])
+@pytest.mark.parametrize("bs", [16, 32, 48, 256])
 def test_group_dim_block_variants(pkv, G, D, bs):
     rng = np.random.default_rng(300 + G * 7 + D + bs)
     lens = [1, 15, 16, 17, 63, 64, 65, 257, 700][: 5 + G // 2]
@@ -192,9 +192,10 @@ def test_group_dim_block_variants(pkv, G, D, bs):
         compare(out, ref, f"G={G} D={D} bs={bs} max_ctas={ctas}")
 
 
-def test_context_len_one_returns_dequantized_v(pkv):
+@pytest.mark.parametrize("bs", [16, 256])
+def test_context_len_one_returns_dequantized_v(pkv, bs):
     rng = np.random.default_rng(22)
-    w = wl.make_workload("rand", B=6, Hq=8, Hkv=2, D=128, bs=16, context_lens=[1] * 6, rng=rng)
+    w = wl.make_workload("rand", B=6, Hq=8, Hkv=2, D=128, bs=bs, context_lens=[1] * 6, rng=rng)
     c = Fp8Case(w)
     out = wl.bf16_bits_to_f32(bits_host(run_step(pkv, c, c.device()))).astype(np.float64)
     for b in range(6):
@@ -204,10 +205,12 @@ def test_context_len_one_returns_dequantized_v(pkv):
             assert (np.abs(out[b, h] - v) <= REL * np.abs(v)).all()
 
 
-def test_nan_codes_in_unread_slots_change_nothing(pkv):
+@pytest.mark.parametrize("bs", [16, 32, 256])
+def test_nan_codes_in_unread_slots_change_nothing(pkv, bs):
+    # G = 4 at D = 128: 32-token boxes where bs allows
     rng = np.random.default_rng(23)
-    lens = [1, 17, 40, 300, 33]
-    w = wl.make_workload("rand", B=5, Hq=8, Hkv=2, D=128, bs=16, context_lens=lens, rng=rng)
+    lens = [1, 17, 40, 300, 33, 5, 48]
+    w = wl.make_workload("rand", B=7, Hq=8, Hkv=2, D=128, bs=bs, context_lens=lens, rng=rng)
     c = Fp8Case(w)
     clean = bits_host(run_step(pkv, c, c.device(), max_ctas=2))
     # mark every slot no sequence reads with the E4M3 NaN code
@@ -221,6 +224,26 @@ def test_nan_codes_in_unread_slots_change_nothing(pkv):
     out = bits_host(run_step(pkv, c, c.device(), max_ctas=2))
     assert np.isfinite(wl.bf16_bits_to_f32(out)).all()
     np.testing.assert_array_equal(out, clean)
+
+
+@pytest.mark.parametrize("bs", [32, 64])
+@pytest.mark.parametrize("D,G,B", [(128, 4, 18), (64, 8, 4000)])
+def test_box_tails_of_32_token_boxes(pkv, D, G, B, bs):
+    """Where three CTAs per SM hold fewer than four stages of 16-token boxes
+    and the block size is a multiple of 32, the kernel takes 32-token boxes
+    (two 16-token MMA tiles each).  G = 4 at D = 128 is such a shape; at
+    D = 64 it takes B in the thousands (the per-sequence arrays share the
+    CTA's shared memory).  Every tail length of a box, including a second
+    half with no valid token, and slices cut at odd box positions."""
+    rng = np.random.default_rng(400 + D + bs)
+    tails = [1, 2, 15, 16, 17, 31, 32, 33, 47, 48, 49, 63, 64, 65, 95, 96, 97, 130]
+    lens = [tails[i % len(tails)] for i in range(B)]
+    w = wl.make_workload("rand", B=B, Hq=2 * G, Hkv=2, D=D, bs=bs, context_lens=lens, rng=rng)
+    c = Fp8Case(w)
+    ref = c.reference()
+    for ctas in (0, 1, 2, 7):
+        out = run_step(pkv, c, c.device(), max_ctas=ctas)
+        compare(out, ref, f"D={D} G={G} B={B} bs={bs} max_ctas={ctas}")
 
 
 def test_fp8_dtype_caches_are_accepted(pkv):
