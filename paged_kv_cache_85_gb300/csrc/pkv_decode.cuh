@@ -636,6 +636,15 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8
             whole = (bm.flags & kStreamFirst) != 0;
         }
         const int nvw = (bm.flags & kBoxLoaded) ? bm.nvalid : 0;
+        // the stage goes back to the producer once the warp's last read of it
+        // (the last V words it needs) is done, before the arithmetic on them
+        bool released = false;
+        auto release = [&]() {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
+            released = true;
+        };
         if (nvw > 0) {
             const uint8_t *Ks = smem + L.kv + ((size_t)stage * 2 * NW + warp) * kBoxBytes;
             const uint8_t *Vs = Ks + (size_t)NW * kBoxBytes;
@@ -702,8 +711,10 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8
                 // with one sub-box, its V words are loaded before the softmax,
                 // whose reductions cover their latency; with two, each after it
                 // (registers)
-                if (NSUB == 1)
+                if (NSUB == 1) {
                     load_v(u, nv);
+                    release();
+                }
                 if (nv < 16) {
                     // tokens past the context: scores -inf
                     if (g >= nv) { sv[u][0] = -INFINITY; sv[u][1] = -INFINITY; }
@@ -748,8 +759,11 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8
                 l1 += p1 + p3;
                 const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
                 const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
-                if (NSUB > 1)
+                if (NSUB > 1) {
                     load_v(u, nv);
+                    if (u == NSUB - 1 || nvw <= 16 * (u + 1))
+                        release();
+                }
                 // ---- O^T += V^T P^T ----
 #pragma unroll
                 for (int w = 0; w < VW; w++) {
@@ -764,9 +778,8 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams &p, uint8
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[stage]);
+        if (!released)
+            release();
 
         if (bm.flags & kPieceLast) {
             float t0 = l0, t1 = l1;
