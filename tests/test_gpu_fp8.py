@@ -246,6 +246,38 @@ def test_box_tails_of_32_token_boxes(pkv, D, G, B, bs):
         compare(out, ref, f"D={D} G={G} B={B} bs={bs} max_ctas={ctas}")
 
 
+@pytest.mark.parametrize("bs", [16, 32])
+def test_bad_block_drops_only_its_tokens(pkv, bs):
+    """A bad block id in a table drops that block's tokens from the softmax
+    and flags PKV_FLAG_BAD_BLOCK (G = 4, D = 128: 16-token boxes at bs = 16,
+    32-token boxes at bs = 32).  Decode attention does not depend on token
+    order, so the expected result is the oracle's over the table without
+    that block."""
+    rng = np.random.default_rng(500 + bs)
+    lens = [100, 37, 260, 9, 100, 64]
+    w = wl.make_workload("rand", B=len(lens), Hq=8, Hkv=2, D=128, bs=bs, context_lens=lens,
+                         rng=rng)
+    c = Fp8Case(w)
+    ref = c.reference()
+    bad_b, bad_j = 4, 2  # a full block in the middle of a 100-token context
+    tables = w.block_tables.copy()
+    tables[bad_b, bad_j:-1] = w.block_tables[bad_b, bad_j + 1:]
+    tables[bad_b, -1] = -1
+    lens2 = w.context_lens.copy()
+    lens2[bad_b] -= bs
+    ref[bad_b] = oracle.paged_attn_decode_fp8(w.q, c.kc2, c.vc2, tables, lens2, w.scale, c.k_scale,
+                                              c.v_scale)[bad_b]
+    for ctas in (0, 3):
+        d = c.device()
+        bad = d["tables"].clone()
+        bad[bad_b, bad_j] = w.NB + 11
+        d["tables"] = bad
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = run_step(pkv, c, d, max_ctas=ctas, err=err)
+        assert int(err.item()) & pkv.FLAG_BAD_BLOCK
+        compare(out, ref, f"bs={bs} max_ctas={ctas}")
+
+
 def test_fp8_dtype_caches_are_accepted(pkv):
     if not hasattr(torch, "float8_e4m3fn"):
         pytest.skip("no float8_e4m3fn in this torch")
